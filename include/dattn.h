@@ -1,0 +1,191 @@
+/*
+ * dattn.h -- C ABI of libdattn: single-query (decode-step) scaled dot-product
+ * attention against an f16 KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the one defined by the two kernels of "Developing Apple
+ * Metal Kernels in Rust - A Deep Dive Through Attention", section "The MSL,
+ * briefly":
+ *   attention_qk_f16:  score[h,pos] = (sum_i Q[h,i] * K_cache[pos,h,i]) / sqrt(head_dim),
+ *                      -infinity where pos > current_pos;
+ *   attention_pv_f16:  out[h,d] = sum_pos softmax(score[h,:])[pos] * V_cache[pos,h,d],
+ *                      the softmax taken with the row maximum subtracted.
+ * This library adds a leading batch dimension (independent sequences, one
+ * current_pos each) and a fused entry point that never materialises the scores.
+ *
+ * Conventions shared by every entry point
+ *   - f16 tensors are passed as untyped pointers to IEEE binary16 data, dense
+ *     and row-major in the layouts given below, and must be 16-byte aligned
+ *     (the page's allocator hands out 16-byte aligned blocks; section "Testing").
+ *   - Every tensor and current_pos array is a DEVICE pointer on the current CUDA
+ *     device.  The caller owns all buffers and the stream; the library keeps no
+ *     pointer after a call returns (like the page-3 C API, which wraps caller
+ *     buffers and never frees them).
+ *   - Calls are asynchronous: they only enqueue kernels on `stream` (NULL = the
+ *     legacy default stream) and return.  The page's launcher waits after every
+ *     dispatch (section "Commit, wait, and reading results back"); here the
+ *     caller synchronises.  Faults during execution surface at that sync.
+ *   - Arguments are validated on the host before anything is launched; on any
+ *     non-zero return nothing has been written.  dattn_last_error() then gives a
+ *     message for the calling thread.
+ *   - current_pos is uint32 per sequence, the page's `uint` (section "The MSL,
+ *     briefly").  A value >= seq_len masks nothing, exactly as the page's test
+ *     `pos > current_pos` never fires then: the live length is
+ *     L = min(current_pos, seq_len - 1) + 1.  The library never reads
+ *     current_pos on the host.
+ */
+#ifndef DATTN_H
+#define DATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (identical to cudaStream_t / CUstream). */
+typedef struct CUstream_st *dattn_stream_t;
+
+/* Status codes returned by every int-returning entry point. */
+enum dattn_status {
+    DATTN_OK = 0,
+    DATTN_ERR_INVALID_ARG = -1, /* null pointer, non-positive size, bad num_splits */
+    DATTN_ERR_UNSUPPORTED = -2, /* head_dim not a multiple of 8 or above 256       */
+    DATTN_ERR_MISALIGNED = -3,  /* a tensor pointer is not 16-byte aligned          */
+    DATTN_ERR_WORKSPACE = -4,   /* workspace missing, misaligned or too small       */
+    DATTN_ERR_CUDA = -5,        /* a CUDA runtime call or kernel launch failed      */
+    DATTN_ERR_TIMEOUT = -6      /* a kernel gave up waiting on its own pipeline     */
+};
+
+/* Library version: major*10000 + minor*100 + patch. */
+int dattn_version(void);
+
+/* Static string naming a status code. */
+const char *dattn_status_string(int status);
+
+/* Message describing the last non-OK return on the calling thread ("" if none). */
+const char *dattn_last_error(void);
+
+/*
+ * Execution plan of the fused decode for a shape on the current device: how the
+ * KV range is split across CTAs.  Filled by dattn_decode_plan(); informational.
+ */
+typedef struct dattn_plan {
+    int num_splits;      /* position ranges per (sequence, head group)           */
+    int split_len;       /* positions per range (the last one may be shorter)    */
+    int heads_per_cta;   /* heads one CTA handles                                */
+    int head_groups;     /* ceil(n_heads / heads_per_cta)                        */
+    int stage_positions; /* positions per shared-memory pipeline stage           */
+    int stages;          /* pipeline depth                                       */
+    int threads_per_cta;
+    int smem_bytes;      /* dynamic shared memory per CTA                        */
+    int ctas_per_sm;     /* resident CTAs per SM at that shared-memory size      */
+    int sm_count;
+    long long ctas;      /* grid size of the split-K kernel                      */
+    size_t workspace_bytes;
+} dattn_plan;
+
+/*
+ * Plan the fused decode for (batch, n_heads, head_dim, seq_len) on the current
+ * device.  num_splits = 0 lets the library choose (a cost model over the SM
+ * count, keyed on seq_len x batch x n_heads); a positive value forces that many
+ * position ranges per sequence (clamped to seq_len and to 16384).
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA (device query failed).
+ */
+int dattn_decode_plan(int batch, int n_heads, int head_dim, int seq_len, int num_splits,
+                      dattn_plan *plan);
+
+/*
+ * Workspace that dattn_decode_f16_ex needs for this shape and num_splits on the
+ * current device, in bytes (0 when a single range covers every sequence).
+ * The workspace holds fp32 partial softmax states (m, l, acc[head_dim]) per
+ * (sequence, head, range); it is scratch, rewritten by every call.
+ * Errors: as dattn_decode_plan, plus INVALID_ARG for a null `bytes`.
+ */
+int dattn_decode_workspace_bytes(int batch, int n_heads, int head_dim, int seq_len,
+                                 int num_splits, size_t *bytes);
+
+/*
+ * Fused decode attention with a caller-provided workspace.
+ *
+ *   Q            [batch, n_heads, head_dim]            f16, device
+ *   K_cache      [batch, seq_len, n_heads, head_dim]   f16, device
+ *   V_cache      [batch, seq_len, n_heads, head_dim]   f16, device
+ *   out          [batch, n_heads, head_dim]            f16, device (written)
+ *   current_pos  [batch]                               uint32, device
+ *   workspace    device scratch, 16-byte aligned, >= dattn_decode_workspace_bytes
+ *                (may be NULL when that is 0)
+ *   num_splits   0 = library heuristic, > 0 forces the split count
+ *
+ * For each sequence b and head h, with L = min(current_pos[b], seq_len-1) + 1:
+ *   out[b,h,:] = sum_{p<L} softmax_p(Q[b,h,:].K[b,p,h,:] / sqrt(head_dim)) V[b,p,h,:]
+ * computed with fp32 accumulation and an online (running max/sum) softmax, then
+ * rounded to f16 (round to nearest even).  Positions p >= L are never read: the
+ * page's -infinity score gives them weight exactly zero.  The KV range of each
+ * sequence is split across CTAs and the partial softmax states are merged by a
+ * second kernel (log-sum-exp merge), both enqueued on `stream`.
+ *
+ * Concurrent calls on different streams need different workspaces.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA.
+ */
+int dattn_decode_f16_ex(const void *Q, const void *K_cache, const void *V_cache, void *out,
+                        int batch, int n_heads, int head_dim, int seq_len,
+                        const uint32_t *current_pos, void *workspace, size_t workspace_bytes,
+                        int num_splits, dattn_stream_t stream);
+
+/*
+ * Fused decode attention with the library's own workspace: same operation and
+ * arguments as dattn_decode_f16_ex with num_splits = 0.  The workspace is owned
+ * by the library, one per (device, stream), grown on demand with cudaMalloc
+ * (serialised by a mutex) and kept until process exit; a call that has to grow
+ * it synchronises the device first.  Make the first call for the largest shape
+ * outside any CUDA graph capture.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, CUDA.
+ */
+int dattn_decode_f16(const void *Q, const void *K_cache, const void *V_cache, void *out,
+                     int batch, int n_heads, int head_dim, int seq_len,
+                     const uint32_t *current_pos, dattn_stream_t stream);
+
+/*
+ * The page's first dispatch, attention_qk_f16, batched ("The MSL, briefly"):
+ *   scores[b,h,p] = half( (fp32 sum over i in index order of Q[b,h,i]*K[b,p,h,i],
+ *                          each product and each sum rounded to fp32)
+ *                         * (1.0f / sqrtf(head_dim)) )        for p <= current_pos[b]
+ *   scores[b,h,p] = -infinity                                 for p >  current_pos[b]
+ *   scores  [batch, n_heads, seq_len] f16, device (written)
+ * Kept for cross-checking the fused path against the page's two-dispatch form.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, CUDA.
+ */
+int dattn_qk_f16(const void *Q, const void *K_cache, void *scores, int batch, int n_heads,
+                 int head_dim, int seq_len, const uint32_t *current_pos,
+                 dattn_stream_t stream);
+
+/*
+ * The page's second dispatch, attention_pv_f16, batched: per (b,h), fp32 max of
+ * the scores row, fp32 sum of expf(score - max), then
+ *   out[b,h,d] = half( sum over all seq_len positions p of
+ *                      (expf(score[b,h,p] - max) / sum) * V[b,p,h,d] ).
+ * Masking is carried by -infinity scores (weight 0); as on the page every
+ * position is multiplied in, so a NaN in V at a zero-weight position propagates.
+ *   scores [batch, n_heads, seq_len] f16, device;  out [batch, n_heads, head_dim]
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, CUDA.
+ */
+int dattn_pv_f16(const void *scores, const void *V_cache, void *out, int batch, int n_heads,
+                 int head_dim, int seq_len, dattn_stream_t stream);
+
+/*
+ * Device-side error word of the current device.  Every wait inside the fused
+ * kernel's shared-memory pipeline is bounded (about one second); a wait that
+ * runs out records a code here, abandons its CTA's output and returns instead
+ * of hanging the GPU.  This call synchronises the device, returns DATTN_OK if
+ * no kernel has recorded an error since the last clear and DATTN_ERR_TIMEOUT
+ * otherwise, and resets the word when `clear` is non-zero.
+ * Errors: TIMEOUT, CUDA.
+ */
+int dattn_device_error(int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DATTN_H */

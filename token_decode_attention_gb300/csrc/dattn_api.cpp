@@ -1,0 +1,460 @@
+// dattn_api.cpp -- the C ABI declared in include/dattn.h.
+//
+// Host side of the library: argument validation (before anything is
+// launched), the split-K plan (a small cost model over the SM count), the
+// library-owned workspace of dattn_decode_f16, status codes and per-thread
+// error messages.  The arithmetic of the operation runs only in the CUDA
+// kernels (decode_splitk.cu, combine.cu, split_calls.cu).
+#include "dattn.h"
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <unordered_map>
+
+#include "dattn_internal.h"
+
+namespace {
+
+using dattn::DecodeVariant;
+
+constexpr int kVersion = 10000;        // 1.0.0
+constexpr int kMaxSplits = 16384;      // position ranges per sequence
+constexpr int kMaxHeadDim = 256;
+constexpr int kMaxHeadsPerLaneGroup = 4;  // register slots per lane group (KMAX)
+constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
+constexpr int kStageTargetBytes = 32 * 1024;
+constexpr int kTwoPerSmBudget = 110 * 1024;
+constexpr double kModelBandwidth = 6.5e12;  // bytes/s used by the split cost model
+constexpr double kCtaOverheadS = 1.5e-6;    // pipeline fill per CTA wave
+constexpr double kCombineLaunchS = 2.0e-6;
+
+thread_local std::string g_last_error;
+
+int fail(int status, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return status;
+}
+
+int fail_cuda(cudaError_t e, const char *what) {
+    return fail(DATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- device info
+
+struct DeviceInfo {
+    int sms = 0;
+    int max_smem_optin = 0;
+    unsigned *err_word = nullptr;
+};
+
+std::mutex g_dev_mutex;
+std::unordered_map<int, DeviceInfo> g_devices;
+
+int current_device(int *dev) {
+    const cudaError_t e = cudaGetDevice(dev);
+    return e == cudaSuccess ? DATTN_OK : fail_cuda(e, "cudaGetDevice");
+}
+
+// Device properties and one-time kernel configuration for the current device.
+int device_info(DeviceInfo *out) {
+    int dev = 0;
+    if (int st = current_device(&dev)) return st;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    auto it = g_devices.find(dev);
+    if (it != g_devices.end()) {
+        *out = it->second;
+        return DATTN_OK;
+    }
+    DeviceInfo di;
+    cudaError_t e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute(SM count)");
+    e = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute(smem opt-in)");
+    e = dattn::decode_configure_smem(di.max_smem_optin);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(split-K kernel)");
+    e = dattn::combine_configure_smem(di.max_smem_optin);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(combine kernel)");
+    e = dattn::device_error_word(&di.err_word);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(error word)");
+    g_devices[dev] = di;
+    *out = di;
+    return DATTN_OK;
+}
+
+// --------------------------------------------------------------------- plans
+
+struct Plan {
+    DecodeVariant v{};
+    int HG = 0, NHG = 0, PHI = 0, P = 0, NST = 0, NS = 0, chunk = 0;
+    int smem = 0, bar_offset = 0, ctas_per_sm = 0, sms = 0;
+    long long ctas = 0;
+    size_t ws_acc_bytes = 0, ws_bytes = 0;
+};
+
+int next_pow2(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+int validate_dims(int B, int H, int D, int S) {
+    if (B <= 0 || H <= 0 || D <= 0 || S <= 0)
+        return fail(DATTN_ERR_INVALID_ARG,
+                    "sizes must be positive (batch=%d n_heads=%d head_dim=%d seq_len=%d)", B, H,
+                    D, S);
+    if (D % 8 != 0 || D > kMaxHeadDim)
+        return fail(DATTN_ERR_UNSUPPORTED, "head_dim=%d: must be a multiple of 8 and <= %d", D,
+                    kMaxHeadDim);
+    // element counts of the largest tensor must stay far inside int64
+    const double elems = static_cast<double>(B) * S * H * D;
+    if (elems > 4.0e18)
+        return fail(DATTN_ERR_INVALID_ARG, "KV cache of %.3g elements is too large", elems);
+    return DATTN_OK;
+}
+
+using PlanKey = std::tuple<int, int, int, int, int, int>;
+std::mutex g_plan_mutex;
+std::map<PlanKey, Plan> g_plans;
+
+// Choose the number of position ranges per sequence: the smallest modelled time
+// over candidate split counts, where a launch costs waves x (range bytes over
+// one CTA slot's share of HBM bandwidth + pipeline fill), plus the combine
+// kernel and its workspace traffic when there is more than one range.
+int choose_splits(const Plan &p, int B, int H, int D, int S) {
+    const long long slots = static_cast<long long>(p.sms) * p.ctas_per_sm;
+    const double slot_bw = kModelBandwidth / static_cast<double>(slots);
+    const double bytes_pos = static_cast<double>(p.HG) * D * 4.0;
+    const long long units = static_cast<long long>(B) * p.NHG;
+    const int ns_max = static_cast<int>(std::min<long long>({S, kMaxSplits, 8 * slots}));
+    int best = 1;
+    double best_t = INFINITY;
+    for (int ns = 1; ns <= ns_max; ++ns) {
+        const int chunk = (S + ns - 1) / ns;
+        if (ns > 1 && chunk < p.P) break;  // every range holds at least one full stage
+        const int nse = (S + chunk - 1) / chunk;
+        if (nse != ns) continue;
+        const long long ctas = units * nse;
+        const double waves = std::ceil(static_cast<double>(ctas) / static_cast<double>(slots));
+        double t = waves * (chunk * bytes_pos / slot_bw + kCtaOverheadS);
+        if (nse > 1)
+            t += kCombineLaunchS +
+                 static_cast<double>(B) * H * nse * (D + 2) * 4.0 * 2.0 / kModelBandwidth;
+        if (t < best_t * (1.0 - 1e-9)) {
+            best_t = t;
+            best = nse;
+        }
+    }
+    return best;
+}
+
+int make_plan(int B, int H, int D, int S, int num_splits, Plan *out) {
+    if (int st = validate_dims(B, H, D, S)) return st;
+    if (num_splits < 0)
+        return fail(DATTN_ERR_INVALID_ARG, "num_splits=%d must be >= 0", num_splits);
+    DeviceInfo di;
+    if (int st = device_info(&di)) return st;
+    int dev = 0;
+    if (int st = current_device(&dev)) return st;
+    const PlanKey key{dev, B, H, D, S, num_splits};
+    {
+        std::lock_guard<std::mutex> lock(g_plan_mutex);
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) {
+            *out = it->second;
+            return DATTN_OK;
+        }
+    }
+    Plan p;
+    p.sms = di.sms;
+    const int bdx = std::min(32, next_pow2(D / 8));
+    const int bdy = 32 / bdx;
+    const int nlg = dattn::kConsumerWarps * bdy;
+    int hg_max = std::min(nlg * kMaxHeadsPerLaneGroup, std::max(1, kMaxRowBytesKV / (D * 4)));
+    p.NHG = (H + hg_max - 1) / hg_max;
+    p.HG = (H + p.NHG - 1) / p.NHG;
+    p.PHI = p.HG >= nlg ? 1 : std::min(32, nlg / p.HG);
+    const int kmax = (p.HG * p.PHI + nlg - 1) / nlg;
+    p.v = DecodeVariant{bdx, kmax};
+    const int row_bytes = p.HG * D * 2;
+    int P = std::max(1, std::min(256, kStageTargetBytes / 2 / row_bytes));
+    P = std::max(p.PHI, P / p.PHI * p.PHI);
+    p.P = P;
+    const int stage_bytes = 2 * P * row_bytes;
+    const int merge_bytes = p.HG * p.PHI * (D + 2) * 4;
+    int nst = kTwoPerSmBudget / stage_bytes;
+    if (nst < 2) nst = (di.max_smem_optin - 1024) / stage_bytes;
+    p.NST = std::max(2, std::min(8, nst));
+    p.bar_offset = round_up(std::max(p.NST * stage_bytes, merge_bytes), 128);
+    p.smem = p.bar_offset + p.NST * 16 + 16;
+    if (p.smem > di.max_smem_optin)
+        return fail(DATTN_ERR_UNSUPPORTED, "shape needs %d B of shared memory (limit %d)",
+                    p.smem, di.max_smem_optin);
+    cudaError_t e = dattn::decode_occupancy(p.v, p.smem, &p.ctas_per_sm);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (p.ctas_per_sm < 1)
+        return fail(DATTN_ERR_UNSUPPORTED, "split-K kernel does not fit on an SM");
+    int ns = num_splits > 0 ? std::min({num_splits, S, kMaxSplits})
+                            : choose_splits(p, B, H, D, S);
+    p.chunk = (S + ns - 1) / ns;
+    p.NS = (S + p.chunk - 1) / p.chunk;
+    p.ctas = static_cast<long long>(B) * p.NHG * p.NS;
+    if (p.ctas > 0x7fffffffLL)
+        return fail(DATTN_ERR_UNSUPPORTED, "grid of %lld CTAs is too large", p.ctas);
+    if (p.NS > 1) {
+        const size_t rows = static_cast<size_t>(B) * H * p.NS;
+        p.ws_acc_bytes = (rows * D * sizeof(float) + 255) / 256 * 256;
+        p.ws_bytes = p.ws_acc_bytes + rows * sizeof(float2);
+        if (dattn::combine_smem_bytes(p.NS, D) > static_cast<size_t>(di.max_smem_optin))
+            return fail(DATTN_ERR_UNSUPPORTED, "num_splits=%d too large for the combine", p.NS);
+    }
+    {
+        std::lock_guard<std::mutex> lock(g_plan_mutex);
+        g_plans[key] = p;
+    }
+    *out = p;
+    return DATTN_OK;
+}
+
+int check_tensor(const void *p, const char *name) {
+    if (p == nullptr) return fail(DATTN_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!aligned16(p)) return fail(DATTN_ERR_MISALIGNED, "%s is not 16-byte aligned", name);
+    return DATTN_OK;
+}
+
+int check_cur_pos(const uint32_t *cp) {
+    if (cp == nullptr) return fail(DATTN_ERR_INVALID_ARG, "current_pos is NULL");
+    if ((reinterpret_cast<uintptr_t>(cp) & 3u) != 0)
+        return fail(DATTN_ERR_MISALIGNED, "current_pos is not 4-byte aligned");
+    return DATTN_OK;
+}
+
+int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, void *out, int B,
+                  int H, int D, int S, const uint32_t *cur_pos, void *workspace,
+                  cudaStream_t stream) {
+    DeviceInfo di;
+    if (int st = device_info(&di)) return st;
+    dattn::DecodeArgs a{};
+    a.Q = Q;
+    a.K = K;
+    a.V = V;
+    a.out = out;
+    a.cur_pos = cur_pos;
+    a.ws_acc = p.NS > 1 ? static_cast<float *>(workspace) : nullptr;
+    a.ws_ml = p.NS > 1
+                  ? reinterpret_cast<float2 *>(static_cast<char *>(workspace) + p.ws_acc_bytes)
+                  : nullptr;
+    a.err = di.err_word;
+    a.B = B;
+    a.H = H;
+    a.D = D;
+    a.S = S;
+    a.heads_per_cta = p.HG;
+    a.head_groups = p.NHG;
+    a.phases = p.PHI;
+    a.stage_pos = p.P;
+    a.stages = p.NST;
+    a.num_splits = p.NS;
+    a.split_len = p.chunk;
+    a.bar_offset = p.bar_offset;
+    a.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    cudaError_t e = dattn::launch_decode_splitk(a, p.v, p.ctas, p.smem, stream);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e, "split-K kernel launch");
+    if (p.NS > 1) {
+        dattn::CombineArgs c{};
+        c.ws_acc = a.ws_acc;
+        c.ws_ml = a.ws_ml;
+        c.cur_pos = cur_pos;
+        c.out = out;
+        c.B = B;
+        c.H = H;
+        c.D = D;
+        c.S = S;
+        c.num_splits = p.NS;
+        c.split_len = p.chunk;
+        e = dattn::launch_combine(c, stream);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) return fail_cuda(e, "combine kernel launch");
+    }
+    return DATTN_OK;
+}
+
+// Library-owned workspaces of dattn_decode_f16, one per (device, stream).
+struct OwnedWorkspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mutex;
+std::map<std::pair<int, cudaStream_t>, OwnedWorkspace> g_workspaces;
+
+}  // namespace
+
+extern "C" {
+
+int dattn_version(void) { return kVersion; }
+
+const char *dattn_status_string(int status) {
+    switch (status) {
+        case DATTN_OK: return "DATTN_OK";
+        case DATTN_ERR_INVALID_ARG: return "DATTN_ERR_INVALID_ARG";
+        case DATTN_ERR_UNSUPPORTED: return "DATTN_ERR_UNSUPPORTED";
+        case DATTN_ERR_MISALIGNED: return "DATTN_ERR_MISALIGNED";
+        case DATTN_ERR_WORKSPACE: return "DATTN_ERR_WORKSPACE";
+        case DATTN_ERR_CUDA: return "DATTN_ERR_CUDA";
+        case DATTN_ERR_TIMEOUT: return "DATTN_ERR_TIMEOUT";
+        default: return "DATTN_ERR_UNKNOWN";
+    }
+}
+
+const char *dattn_last_error(void) { return g_last_error.c_str(); }
+
+int dattn_decode_plan(int batch, int n_heads, int head_dim, int seq_len, int num_splits,
+                      dattn_plan *plan) {
+    if (plan == nullptr) return fail(DATTN_ERR_INVALID_ARG, "plan is NULL");
+    Plan p;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_splits, &p)) return st;
+    plan->num_splits = p.NS;
+    plan->split_len = p.chunk;
+    plan->heads_per_cta = p.HG;
+    plan->head_groups = p.NHG;
+    plan->stage_positions = p.P;
+    plan->stages = p.NST;
+    plan->threads_per_cta = dattn::kDecodeThreads;
+    plan->smem_bytes = p.smem;
+    plan->ctas_per_sm = p.ctas_per_sm;
+    plan->sm_count = p.sms;
+    plan->ctas = p.ctas;
+    plan->workspace_bytes = p.ws_bytes;
+    return DATTN_OK;
+}
+
+int dattn_decode_workspace_bytes(int batch, int n_heads, int head_dim, int seq_len,
+                                 int num_splits, size_t *bytes) {
+    if (bytes == nullptr) return fail(DATTN_ERR_INVALID_ARG, "bytes is NULL");
+    Plan p;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_splits, &p)) return st;
+    *bytes = p.ws_bytes;
+    return DATTN_OK;
+}
+
+int dattn_decode_f16_ex(const void *Q, const void *K_cache, const void *V_cache, void *out,
+                        int batch, int n_heads, int head_dim, int seq_len,
+                        const uint32_t *current_pos, void *workspace, size_t workspace_bytes,
+                        int num_splits, dattn_stream_t stream) {
+    if (int st = check_tensor(Q, "Q")) return st;
+    if (int st = check_tensor(K_cache, "K_cache")) return st;
+    if (int st = check_tensor(V_cache, "V_cache")) return st;
+    if (int st = check_tensor(out, "out")) return st;
+    if (int st = check_cur_pos(current_pos)) return st;
+    if (int st = validate_dims(batch, n_heads, head_dim, seq_len)) return st;
+    if (num_splits < 0)
+        return fail(DATTN_ERR_INVALID_ARG, "num_splits=%d must be >= 0", num_splits);
+    Plan p;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_splits, &p)) return st;
+    if (p.ws_bytes > 0) {
+        if (workspace == nullptr)
+            return fail(DATTN_ERR_WORKSPACE, "workspace of %zu bytes required, got NULL",
+                        p.ws_bytes);
+        if (!aligned16(workspace))
+            return fail(DATTN_ERR_WORKSPACE, "workspace is not 16-byte aligned");
+        if (workspace_bytes < p.ws_bytes)
+            return fail(DATTN_ERR_WORKSPACE, "workspace of %zu bytes required, got %zu",
+                        p.ws_bytes, workspace_bytes);
+    }
+    return launch_decode(p, Q, K_cache, V_cache, out, batch, n_heads, head_dim, seq_len,
+                         current_pos, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dattn_decode_f16(const void *Q, const void *K_cache, const void *V_cache, void *out,
+                     int batch, int n_heads, int head_dim, int seq_len,
+                     const uint32_t *current_pos, dattn_stream_t stream) {
+    if (int st = check_tensor(Q, "Q")) return st;
+    if (int st = check_tensor(K_cache, "K_cache")) return st;
+    if (int st = check_tensor(V_cache, "V_cache")) return st;
+    if (int st = check_tensor(out, "out")) return st;
+    if (int st = check_cur_pos(current_pos)) return st;
+    Plan p;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, 0, &p)) return st;
+    void *ws = nullptr;
+    if (p.ws_bytes > 0) {
+        int dev = 0;
+        if (int st = current_device(&dev)) return st;
+        std::lock_guard<std::mutex> lock(g_ws_mutex);
+        OwnedWorkspace &w = g_workspaces[{dev, reinterpret_cast<cudaStream_t>(stream)}];
+        if (w.bytes < p.ws_bytes) {
+            cudaError_t e = cudaDeviceSynchronize();
+            if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize (workspace grow)");
+            if (w.ptr != nullptr) cudaFree(w.ptr);
+            w.ptr = nullptr;
+            w.bytes = 0;
+            e = cudaMalloc(&w.ptr, p.ws_bytes);
+            if (e != cudaSuccess) return fail_cuda(e, "cudaMalloc (workspace)");
+            w.bytes = p.ws_bytes;
+        }
+        ws = w.ptr;
+    }
+    return launch_decode(p, Q, K_cache, V_cache, out, batch, n_heads, head_dim, seq_len,
+                         current_pos, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dattn_qk_f16(const void *Q, const void *K_cache, void *scores, int batch, int n_heads,
+                 int head_dim, int seq_len, const uint32_t *current_pos,
+                 dattn_stream_t stream) {
+    if (int st = check_tensor(Q, "Q")) return st;
+    if (int st = check_tensor(K_cache, "K_cache")) return st;
+    if (int st = check_tensor(scores, "scores")) return st;
+    if (int st = check_cur_pos(current_pos)) return st;
+    if (int st = validate_dims(batch, n_heads, head_dim, seq_len)) return st;
+    const cudaError_t e = dattn::launch_qk(Q, K_cache, scores, batch, n_heads, head_dim, seq_len,
+                                           current_pos, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DATTN_OK : fail_cuda(e, "qk kernel launch");
+}
+
+int dattn_pv_f16(const void *scores, const void *V_cache, void *out, int batch, int n_heads,
+                 int head_dim, int seq_len, dattn_stream_t stream) {
+    if (int st = check_tensor(scores, "scores")) return st;
+    if (int st = check_tensor(V_cache, "V_cache")) return st;
+    if (int st = check_tensor(out, "out")) return st;
+    if (int st = validate_dims(batch, n_heads, head_dim, seq_len)) return st;
+    const cudaError_t e = dattn::launch_pv(scores, V_cache, out, batch, n_heads, head_dim,
+                                           seq_len, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DATTN_OK : fail_cuda(e, "pv kernel launch");
+}
+
+int dattn_device_error(int clear) {
+    DeviceInfo di;
+    if (int st = device_info(&di)) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+    unsigned word = 0;
+    e = cudaMemcpy(&word, di.err_word, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemcpy (error word)");
+    if (clear && word != 0) {
+        e = cudaMemset(di.err_word, 0, sizeof(unsigned));
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return fail_cuda(e, "cudaMemset (error word)");
+    }
+    if (word != 0)
+        return fail(DATTN_ERR_TIMEOUT, "a kernel gave up on a pipeline wait (code 0x%x)", word);
+    return DATTN_OK;
+}
+
+}  // extern "C"
