@@ -1,0 +1,445 @@
+"""Benchmark: decode-attention effective HBM GB/s and query-heads/s on GB300.
+
+One step = one fused decode call (split-K kernel + combine) over one batch of
+synthetic input of the chosen workload (default: the 7B-class decode step,
+B=1 H=32 D=128 S=4096 current_pos=4095).  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--no-sweep] [--cpu-seconds T]
+
+Timing: W untimed warm-up steps, a ~1 s untimed load soak (so clocks settle and
+can be sampled), then exactly K steps bracketed by a barrier and
+torch.cuda.synchronize() with CUDA events on the launching stream; max over
+ranks.  Workloads whose K/V fit in L2 rotate through enough independent input
+sets that their total exceeds 4x L2, so no step reads inputs left in L2 by the
+previous one.  N > 1 runs one independent replica per GPU (weak scaling): the
+path shards by sequence with no data exchange.
+
+--impl reference times the CPU oracle (the plain fp64 restatement of the
+method) on this host's cores, on the same workload, metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from token_decode_attention_gb300.workloads import (  # noqa: E402
+    WORKLOADS, algorithmic_bytes, make_inputs)
+
+METRIC = "decode-attention effective HBM GB/s (% of GB300 peak) and query-heads/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ------------------------------------------------------------------ helpers
+
+def hbm_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "token_decode_attention_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per call from a committed ncu summary, if it matches these sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    entry = rec.get(workload)
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_call")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------- our arm
+
+class Replica:
+    """Input sets, outputs and workspace of one workload on one GPU."""
+
+    def __init__(self, name: str, device, l2_bytes: int):
+        import token_decode_attention_gb300 as dattn
+        self.dattn = dattn
+        self.w = w = WORKLOADS[name]
+        self.device = device
+        kv = w.kv_bytes()
+        self.sets_n = 1 if kv >= 4 * l2_bytes else min(4096, math.ceil(4 * l2_bytes / kv) + 1)
+        base = make_inputs(w, device)
+        self.cp_host = base["cur_pos_host"]
+        self.sets = [base]
+        for i in range(1, self.sets_n):
+            self.sets.append({"q": base["q"].clone(), "k": base["k"].clone(),
+                              "v": base["v"].clone(), "cur_pos": base["cur_pos"]})
+        self.outs = [torch.empty((w.batch, w.n_heads, w.head_dim), dtype=torch.float16,
+                                 device=device) for _ in range(self.sets_n)]
+        self.plan = dattn.dattn_decode_plan(w.batch, w.n_heads, w.head_dim, w.seq_len, 0)
+        nbytes = max(16, self.plan["workspace_bytes"])
+        self.ws = torch.empty((nbytes,), dtype=torch.uint8, device=device)
+        self.bytes_per_step = algorithmic_bytes(w.batch, w.n_heads, w.head_dim, w.seq_len,
+                                                self.cp_host)
+        self.launches_per_step = 1 + (1 if self.plan["num_splits"] > 1 else 0)
+        self.l2_note = (f"inputs larger than L2 ({kv / 2**30:.2f} GiB K+V)" if self.sets_n == 1
+                        else f"rotating {self.sets_n} input sets, {self.sets_n * kv / 2**30:.2f}"
+                             f" GiB K+V in total (> 4x L2)")
+
+    def step(self, i: int, stream):
+        x = self.sets[i % self.sets_n]
+        self.dattn.dattn_decode_f16_ex(x["q"], x["k"], x["v"], self.outs[i % self.sets_n],
+                                       x["cur_pos"], self.ws, 0, stream)
+
+    def timed(self, steps: int, warmup: int, stream, world: int, soak_s: float = 1.0,
+              sampler: ClockSampler | None = None):
+        with torch.cuda.stream(stream):
+            for i in range(warmup):
+                self.step(i, stream)
+            torch.cuda.synchronize()
+            # untimed load soak: clocks settle, and the sampler sees the GPU busy
+            if sampler is not None:
+                sampler.start()
+            t_end = time.time() + soak_s
+            i = 0
+            while time.time() < t_end:
+                for _ in range(20):
+                    self.step(i, stream)
+                    i += 1
+                stream.synchronize()
+            barrier(world)
+            torch.cuda.synchronize()
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            for i in range(steps):
+                self.step(i, stream)
+            end.record(stream)
+            torch.cuda.synchronize()
+            barrier(world)
+        clocks = sampler.stop() if sampler is not None else None
+        ms = start.elapsed_time(end)
+        return ms, clocks
+
+    def e2e(self, steps: int, warmup: int, stream):
+        """Same metric through the public API with host buffers: each step copies
+        Q, the new token's K/V row and current_pos from pinned host memory,
+        appends the K/V row at current_pos, runs the decode and reads out back
+        into pinned host memory.  The KV cache itself is device-resident state."""
+        w = self.w
+        x = self.sets[0]
+        B, H, D = w.batch, w.n_heads, w.head_dim
+        q_h = x["q"].cpu().pin_memory()
+        cp_h = x["cur_pos"].cpu().pin_memory()
+        last = np.minimum(self.cp_host.astype(np.int64), w.seq_len - 1)
+        knew_h = torch.stack([x["k"][b, int(last[b])] for b in range(B)]).cpu().pin_memory()
+        vnew_h = torch.stack([x["v"][b, int(last[b])] for b in range(B)]).cpu().pin_memory()
+        out_h = torch.empty((B, H, D), dtype=torch.float16).pin_memory()
+        q_d = torch.empty_like(x["q"])
+        cp_d = torch.empty_like(x["cur_pos"])
+        knew_d = torch.empty((B, H, D), dtype=torch.float16, device=self.device)
+        vnew_d = torch.empty_like(knew_d)
+        rows = torch.from_numpy(np.arange(B) * w.seq_len + last).to(self.device)
+        kflat = x["k"].view(B * w.seq_len, H, D)
+        vflat = x["v"].view(B * w.seq_len, H, D)
+        out_d = self.outs[0]
+        h2d = (q_h.numel() + knew_h.numel() + vnew_h.numel()) * 2 + cp_h.numel() * 4
+        d2h = out_h.numel() * 2
+
+        def one():
+            q_d.copy_(q_h, non_blocking=True)
+            cp_d.copy_(cp_h, non_blocking=True)
+            knew_d.copy_(knew_h, non_blocking=True)
+            vnew_d.copy_(vnew_h, non_blocking=True)
+            kflat.index_copy_(0, rows, knew_d)
+            vflat.index_copy_(0, rows, vnew_d)
+            self.dattn.dattn_decode_f16_ex(q_d, x["k"], x["v"], out_d, cp_d, self.ws, 0, stream)
+            out_h.copy_(out_d, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                one()
+            torch.cuda.synchronize()
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            t0 = time.perf_counter()
+            start.record(stream)
+            for _ in range(steps):
+                one()
+            end.record(stream)
+            torch.cuda.synchronize()
+            wall = time.perf_counter() - t0
+        ms = start.elapsed_time(end) / steps
+        return {"value": self.bytes_per_step / (ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": ms, "wall_ms_per_step": wall * 1e3 / steps,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "note": "Q, new K/V row and current_pos copied H2D from pinned memory, "
+                        "K/V row appended at current_pos, decode, out copied D2H; "
+                        "the KV cache is device-resident state"}
+
+
+def cpu_baseline(name: str, budget_s: float, max_reps: int = 1000) -> dict:
+    """The CPU oracle, as it stands, on a bounded sample of the workload."""
+    import oracle
+    w = WORKLOADS[name]
+    x = make_inputs(w, "cuda")
+    q, k, v = (x[n].cpu().numpy() for n in ("q", "k", "v"))
+    cp = x["cur_pos_host"]
+    del x
+    nbytes = algorithmic_bytes(w.batch, w.n_heads, w.head_dim, w.seq_len, cp)
+    reps, t0 = 0, time.perf_counter()
+    while reps < max_reps:
+        oracle.decode_f64(q, k, v, cp)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": nbytes * reps / el / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "seconds": el,
+            "query_heads_per_s": w.batch * w.n_heads * reps / el,
+            "sample": f"{reps} full passes of the {name} workload ({w.description}), "
+                      f"fp64 C oracle with OpenMP"}
+
+
+def sweep(device, stream, l2_bytes: int, steps: int, warmup: int, peak: float) -> dict:
+    res = {}
+    for name in ("small", "7b", "ragged", "long", "outlier"):
+        try:
+            r = Replica(name, device, l2_bytes)
+            ms, _ = r.timed(steps, warmup, stream, 1, soak_s=0.2)
+            t = ms * 1e-3 / steps
+            gbs = r.bytes_per_step / t / 1e9
+            res[name] = {"us_per_step": t * 1e6, "GB/s": gbs, "frac_of_measured": gbs / peak,
+                         "frac_of_nominal_8TBs": gbs / NOMINAL_HBM_GBS,
+                         "query_heads_per_s": r.w.batch * r.w.n_heads / t,
+                         "num_splits": r.plan["num_splits"], "ctas": r.plan["ctas"],
+                         "algorithmic_bytes": r.bytes_per_step, "l2": r.l2_note}
+            del r
+        except Exception as e:  # report, keep going
+            res[name] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------------- main
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    w = WORKLOADS[args.workload]
+    # the oracle's inputs: same shapes and recipe, drawn on the host
+    x = make_inputs(w, "cpu")
+    q, k, v = (x[n].numpy() for n in ("q", "k", "v"))
+    cp = x["cur_pos_host"]
+    nbytes = algorithmic_bytes(w.batch, w.n_heads, w.head_dim, w.seq_len, cp)
+    for _ in range(args.warmup):
+        oracle.decode_f64(q, k, v, cp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode_f64(q, k, v, cp)
+    el = time.perf_counter() - t0
+    val = nbytes * args.steps / el / 1e9
+    line = {"metric": METRIC, "value": val, "unit": "GB/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{w.name}: {w.description}", "batch": w.batch,
+                       "n_heads": w.n_heads, "head_dim": w.head_dim, "seq_len": w.seq_len,
+                       "parallelism": "replicas"},
+            "query_heads_per_s": w.batch * w.n_heads * args.steps / el,
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": oracle.max_threads(),
+                             "kind": "oracle",
+                             "sample": f"each step one full pass of the {w.name} workload"},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="7b", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    from token_decode_attention_gb300 import build
+    if rank == 0:
+        build.build()
+    barrier(world)
+    import token_decode_attention_gb300 as dattn
+    dattn.load()
+
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2**20)
+    peak, peak_kind = hbm_peak()
+    stream = torch.cuda.Stream(device=device)
+
+    rep = Replica(args.workload, device, l2)
+    sampler = ClockSampler(local)
+    ms, clocks = rep.timed(args.steps, args.warmup, stream, world, sampler=sampler)
+    ms_max = max_over_ranks(ms, world, device)
+    t_step = ms_max * 1e-3 / args.steps
+    total_bytes = rep.bytes_per_step * world
+    value = total_bytes / t_step / 1e9
+    per_call = rep.bytes_per_step / t_step / 1e9
+    e2e = rep.e2e(args.steps, args.warmup, stream)
+    if dattn.dattn_device_error(clear=True) != 0:
+        raise RuntimeError("device error word set: a kernel gave up on a pipeline wait")
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    w = rep.w
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.description}", "batch": w.batch,
+                   "n_heads": w.n_heads, "head_dim": w.head_dim, "seq_len": w.seq_len,
+                   "current_pos": "per-sequence" if w.current_pos is None else w.current_pos,
+                   "num_splits": rep.plan["num_splits"], "l2": rep.l2_note,
+                   "parallelism": f"replicas x{world}"},
+        "query_heads_per_s": world * w.batch * w.n_heads / t_step,
+        "frac_of_nominal_8TBs": per_call / NOMINAL_HBM_GBS,
+        "roofline": {"bound": "hbm", "achieved": per_call, "peak": peak, "unit": "GB/s",
+                     "frac": per_call / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": recorded_traffic(w.name),
+                     "kernel": "dattn_decode_f16_ex call: decode_splitk_kernel + combine_kernel",
+                     "algorithmic_bytes_per_call": rep.bytes_per_step},
+        "e2e": e2e,
+        "gpu_launches": rep.launches_per_step * args.steps,
+        "clocks": clocks,
+        "plan": rep.plan,
+    }
+    del rep
+    torch.cuda.empty_cache()
+    if world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+        if not args.no_sweep:
+            line["sweep"] = sweep(device, stream, l2, 20, 3, peak)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
