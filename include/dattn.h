@@ -173,6 +173,35 @@ int dattn_qk_f16(const void *Q, const void *K_cache, void *scores, int batch, in
 int dattn_pv_f16(const void *scores, const void *V_cache, void *out, int batch, int n_heads,
                  int head_dim, int seq_len, dattn_stream_t stream);
 
+/* Size of the static scratch array used by dattn_decode_f16_noalloc. */
+#define DATTN_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * Fused decode attention that allocates nothing.  The paper has no counterpart
+ * to this entry point; it exists for callers that cannot call cudaMalloc at
+ * decode time (a runtime that owns all device memory through its own pool, or
+ * code that runs where an allocation is forbidden or would synchronise).
+ *
+ * Same operation and arguments as dattn_decode_f16 (library-chosen split
+ * count).  Instead of a workspace it uses a static device array of
+ * DATTN_NOALLOC_SCRATCH_BYTES (32 MiB) that belongs to the library image: every
+ * GPU on which the library's code is loaded holds that array until the process
+ * exits.  Shapes whose split-K partial states need more than that are rejected
+ * with DATTN_ERR_WORKSPACE before anything is launched; dattn_decode_f16_ex
+ * with a caller workspace handles them.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, with the device current); make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * previous call's contents (nothing in it needs to start at zero): calls whose
+ * executions overlap on the GPU (different streams, or without ordering
+ * between them) race on the scratch and give wrong results.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA.
+ */
+int dattn_decode_f16_noalloc(const void *Q, const void *K_cache, const void *V_cache,
+                             void *out, int batch, int n_heads, int head_dim, int seq_len,
+                             const uint32_t *current_pos, dattn_stream_t stream);
+
 /*
  * Device-side error word of the current device.  Every wait inside the fused
  * kernel's shared-memory pipeline is bounded (about one second); a wait that

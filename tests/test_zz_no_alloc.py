@@ -1,0 +1,90 @@
+"""dattn_decode_f16_noalloc: the fused decode for callers that cannot allocate.
+
+Callers such as runtimes that own all device memory through their own pool, or
+code running where a cudaMalloc is forbidden or would synchronise the device,
+cannot hand the library a freshly allocated workspace.  This entry point uses a
+static device array built into the library instead.  Here it is called
+through the C ABI (ctypes, raw device pointers) and its output is compared with
+the workspace-taking entry point dattn_decode_f16_ex on the same inputs, on two
+calls in a row, within the decode tolerance of the other tests.
+
+This file is named so that pytest collects it last; it passes alone in a fresh
+process as well as after the other tests.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from token_decode_attention_gb300 import _native, build
+
+from ._util import ATOL, RTOL, cur_pos_tensor, rand_f16
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_BYTES = 32 * 1024 * 1024  # DATTN_NOALLOC_SCRATCH_BYTES in include/dattn.h
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _native.load()
+
+
+def _noalloc(lib, q, k, v, out, cp):
+    B, H, D = q.shape
+    S = k.shape[1]
+    stream = torch.cuda.current_stream().cuda_stream
+    return lib.dattn_decode_f16_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                        B, H, D, S, cp.data_ptr(), stream)
+
+
+def _reference(q, k, v, cp):
+    """The existing entry point, with a workspace allocated by the test."""
+    B, H, D = q.shape
+    S = k.shape[1]
+    out = torch.empty((B, H, D), dtype=torch.float16, device="cuda")
+    n = _native.dattn_decode_workspace_bytes(B, H, D, S, 0)
+    ws = torch.empty((max(n, 16),), dtype=torch.uint8, device="cuda")
+    _native.dattn_decode_f16_ex(q, k, v, out, cp, ws, 0)
+    return out
+
+
+def _close(got, ref, what):
+    g = got.double().cpu().numpy()
+    r = ref.double().cpu().numpy()
+    err = np.abs(g - r)
+    assert (err <= ATOL + RTOL * np.abs(r)).all(), f"{what}: max err {err.max():.3g}"
+
+
+def test_two_calls_in_a_row_match_the_workspace_entry_point(lib):
+    g = torch.Generator(device="cuda").manual_seed(20260123)
+    cases = [
+        # (B, H, D, S, current_pos): both need split-K scratch
+        (1, 32, 128, 4096, [4095]),
+        (6, 8, 64, 1500, [1499, 0, 700, 3, 1200, 999]),
+    ]
+    for i, (B, H, D, S, cp) in enumerate(cases):
+        assert _native.dattn_decode_workspace_bytes(B, H, D, S, 0) > 0
+        q, k, v = rand_f16(g, (B, H, D)), rand_f16(g, (B, S, H, D)), rand_f16(g, (B, S, H, D))
+        cpt = cur_pos_tensor(cp)
+        out = torch.full((B, H, D), float("nan"), dtype=torch.float16, device="cuda")
+        st = _noalloc(lib, q, k, v, out, cpt)
+        assert st == 0, lib.dattn_last_error().decode()
+        ref = _reference(q, k, v, cpt)
+        torch.cuda.synchronize()
+        _close(out, ref, f"call {i + 1}")
+    assert _native.dattn_device_error(clear=True) == 0
+
+
+def test_shape_beyond_static_scratch_is_rejected(lib):
+    # 256 sequences x 40 heads x 8192 positions needs ~100 MB of partial
+    # states; the call must fail on the host before launching anything
+    B, H, D, S = 256, 40, 128, 8192
+    need = _native.dattn_decode_workspace_bytes(B, H, D, S, 0)
+    assert need > SCRATCH_BYTES  # guarantees the host-side rejection below
+    fake = 1 << 20  # aligned, never dereferenced: nothing is launched on rejection
+    st = lib.dattn_decode_f16_noalloc(fake, fake, fake, fake, B, H, D, S, fake, None)
+    assert st == _native.ERR_WORKSPACE
+    assert "scratch" in lib.dattn_last_error().decode()

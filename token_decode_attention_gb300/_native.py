@@ -53,6 +53,7 @@ _SIGNATURES = {
     "dattn_decode_f16_ex": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, ctypes.c_size_t, _I, _P],
                             _I),
     "dattn_decode_f16": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P], _I),
+    "dattn_decode_f16_noalloc": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P], _I),
     "dattn_qk_f16": ([_P, _P, _P, _I, _I, _I, _I, _P, _P], _I),
     "dattn_pv_f16": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
     "dattn_device_error": ([_I], _I),

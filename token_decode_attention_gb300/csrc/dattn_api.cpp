@@ -307,6 +307,10 @@ std::map<std::pair<int, cudaStream_t>, OwnedWorkspace> g_workspaces;
 
 }  // namespace
 
+namespace dattn {
+int set_last_error(int status, const char *message) { return fail(status, "%s", message); }
+}  // namespace dattn
+
 extern "C" {
 
 int dattn_version(void) { return kVersion; }

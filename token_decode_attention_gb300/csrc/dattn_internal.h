@@ -81,6 +81,10 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream);
 // Device error word of the current device.
 cudaError_t device_error_word(unsigned **ptr);
 
+// Record `message` as the calling thread's dattn_last_error() text and return
+// `status` (for entry points defined outside dattn_api.cpp).
+int set_last_error(int status, const char *message);
+
 // Page-faithful split calls.
 cudaError_t launch_qk(const void *Q, const void *K, void *scores, int B, int H, int D, int S,
                       const uint32_t *cur_pos, cudaStream_t stream);
