@@ -189,33 +189,53 @@ class Replica:
                                        x["cur_pos"], self.ws, 0, stream)
 
     def timed(self, steps: int, warmup: int, stream, world: int, soak_s: float = 1.0,
-              sampler: ClockSampler | None = None):
+              sampler: ClockSampler | None = None, graph: bool = True):
+        """Device time of exactly `steps` consecutive steps, in ms.
+
+        With graph=True the K steps (rotating input sets) are captured once into
+        a CUDA graph, outside the timed region, and the timed region replays it
+        once: the GPU runs the K decode calls back to back, as a decode loop
+        under graph submission does.  With graph=False the calls are issued
+        eagerly from Python, so host overhead per call is included."""
         with torch.cuda.stream(stream):
             for i in range(warmup):
                 self.step(i, stream)
             torch.cuda.synchronize()
+            g = None
+            if graph:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(steps):
+                        self.step(i, stream)
+                g.replay()
+                torch.cuda.synchronize()
+
+            def run_once():
+                if g is not None:
+                    g.replay()
+                else:
+                    for i in range(steps):
+                        self.step(i, stream)
+
             # untimed load soak: clocks settle, and the sampler sees the GPU busy
             if sampler is not None:
                 sampler.start()
             t_end = time.time() + soak_s
-            i = 0
             while time.time() < t_end:
-                for _ in range(20):
-                    self.step(i, stream)
-                    i += 1
+                run_once()
                 stream.synchronize()
             barrier(world)
             torch.cuda.synchronize()
             start = torch.cuda.Event(enable_timing=True)
             end = torch.cuda.Event(enable_timing=True)
             start.record(stream)
-            for i in range(steps):
-                self.step(i, stream)
+            run_once()
             end.record(stream)
             torch.cuda.synchronize()
             barrier(world)
         clocks = sampler.stop() if sampler is not None else None
         ms = start.elapsed_time(end)
+        del g
         return ms, clocks
 
     def e2e(self, steps: int, warmup: int, stream):
@@ -361,6 +381,10 @@ def main():
     ap.add_argument("--workload", default="7b", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="issue the timed steps from Python instead of a CUDA graph")
+    ap.add_argument("--profile", action="store_true",
+                    help="only warm-up and timed steps of one workload (for ncu captures)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -390,7 +414,17 @@ def main():
 
     rep = Replica(args.workload, device, l2)
     sampler = ClockSampler(local)
-    ms, clocks = rep.timed(args.steps, args.warmup, stream, world, sampler=sampler)
+    if args.profile:
+        ms, _ = rep.timed(args.steps, args.warmup, stream, world, soak_s=0.0,
+                          graph=not args.eager)
+        t = ms * 1e-3 / args.steps
+        print(json.dumps({"profile": args.workload, "ms_per_step": t * 1e3,
+                          "GB/s": rep.bytes_per_step / t / 1e9, "plan": rep.plan}), flush=True)
+        return
+    ms, clocks = rep.timed(args.steps, args.warmup, stream, world, sampler=sampler,
+                           graph=not args.eager)
+    eager_ms, _ = rep.timed(args.steps, 1, stream, world, soak_s=0.0, graph=False)
+    eager_ms = max_over_ranks(eager_ms, world, device)
     ms_max = max_over_ranks(ms, world, device)
     t_step = ms_max * 1e-3 / args.steps
     total_bytes = rep.bytes_per_step * world
@@ -425,6 +459,9 @@ def main():
                      "kernel": "dattn_decode_f16_ex call: decode_splitk_kernel + combine_kernel",
                      "algorithmic_bytes_per_call": rep.bytes_per_step},
         "e2e": e2e,
+        "submission": "eager Python calls" if args.eager else
+                      "one CUDA graph of the K steps, captured before the timed region",
+        "eager_ms_per_step": eager_ms / args.steps,
         "gpu_launches": rep.launches_per_step * args.steps,
         "clocks": clocks,
         "plan": rep.plan,
