@@ -158,7 +158,7 @@ def barrier(world: int):
 class Replica:
     """Input sets, outputs and workspace of one workload on one GPU."""
 
-    def __init__(self, name: str, device, l2_bytes: int):
+    def __init__(self, name: str, device, l2_bytes: int, partitions: int = 0):
         import token_decode_attention_gb300 as dattn
         self.dattn = dattn
         self.w = w = WORKLOADS[name]
@@ -173,12 +173,14 @@ class Replica:
                               "v": base["v"].clone(), "cur_pos": base["cur_pos"]})
         self.outs = [torch.empty((w.batch, w.n_heads, w.head_dim), dtype=torch.float16,
                                  device=device) for _ in range(self.sets_n)]
-        self.plan = dattn.dattn_decode_plan(w.batch, w.n_heads, w.head_dim, w.seq_len, 0)
+        self.partitions = partitions
+        self.plan = dattn.dattn_decode_plan(w.batch, w.n_heads, w.head_dim, w.seq_len,
+                                            partitions)
         nbytes = max(16, self.plan["workspace_bytes"])
         self.ws = torch.empty((nbytes,), dtype=torch.uint8, device=device)
         self.bytes_per_step = algorithmic_bytes(w.batch, w.n_heads, w.head_dim, w.seq_len,
                                                 self.cp_host)
-        self.launches_per_step = 1 + (1 if self.plan["num_splits"] > 1 else 0)
+        self.launches_per_step = 1 + (1 if self.plan["partitions"] > 1 else 0)
         self.l2_note = (f"inputs larger than L2 ({kv / 2**30:.2f} GiB K+V)" if self.sets_n == 1
                         else f"rotating {self.sets_n} input sets, {self.sets_n * kv / 2**30:.2f}"
                              f" GiB K+V in total (> 4x L2)")
@@ -186,7 +188,7 @@ class Replica:
     def step(self, i: int, stream):
         x = self.sets[i % self.sets_n]
         self.dattn.dattn_decode_f16_ex(x["q"], x["k"], x["v"], self.outs[i % self.sets_n],
-                                       x["cur_pos"], self.ws, 0, stream)
+                                       x["cur_pos"], self.ws, self.partitions, stream)
 
     def timed(self, steps: int, warmup: int, stream, world: int, soak_s: float = 1.0,
               sampler: ClockSampler | None = None, graph: bool = True):
@@ -270,7 +272,8 @@ class Replica:
             vnew_d.copy_(vnew_h, non_blocking=True)
             kflat.index_copy_(0, rows, knew_d)
             vflat.index_copy_(0, rows, vnew_d)
-            self.dattn.dattn_decode_f16_ex(q_d, x["k"], x["v"], out_d, cp_d, self.ws, 0, stream)
+            self.dattn.dattn_decode_f16_ex(q_d, x["k"], x["v"], out_d, cp_d, self.ws,
+                                           self.partitions, stream)
             out_h.copy_(out_d, non_blocking=True)
 
         with torch.cuda.stream(stream):
@@ -329,7 +332,7 @@ def sweep(device, stream, l2_bytes: int, steps: int, warmup: int, peak: float) -
             res[name] = {"us_per_step": t * 1e6, "GB/s": gbs, "frac_of_measured": gbs / peak,
                          "frac_of_nominal_8TBs": gbs / NOMINAL_HBM_GBS,
                          "query_heads_per_s": r.w.batch * r.w.n_heads / t,
-                         "num_splits": r.plan["num_splits"], "ctas": r.plan["ctas"],
+                         "partitions": r.plan["partitions"],
                          "algorithmic_bytes": r.bytes_per_step, "l2": r.l2_note}
             del r
         except Exception as e:  # report, keep going
@@ -383,6 +386,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--eager", action="store_true",
                     help="issue the timed steps from Python instead of a CUDA graph")
+    ap.add_argument("--partitions", type=int, default=0,
+                    help="force the number of decode partitions (0 = library choice)")
     ap.add_argument("--profile", action="store_true",
                     help="only warm-up and timed steps of one workload (for ncu captures)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -412,7 +417,7 @@ def main():
     peak, peak_kind = hbm_peak()
     stream = torch.cuda.Stream(device=device)
 
-    rep = Replica(args.workload, device, l2)
+    rep = Replica(args.workload, device, l2, args.partitions)
     sampler = ClockSampler(local)
     if args.profile:
         ms, _ = rep.timed(args.steps, args.warmup, stream, world, soak_s=0.0,
@@ -449,7 +454,7 @@ def main():
         "config": {"workload": f"{w.name}: {w.description}", "batch": w.batch,
                    "n_heads": w.n_heads, "head_dim": w.head_dim, "seq_len": w.seq_len,
                    "current_pos": "per-sequence" if w.current_pos is None else w.current_pos,
-                   "num_splits": rep.plan["num_splits"], "l2": rep.l2_note,
+                   "partitions": rep.plan["partitions"], "l2": rep.l2_note,
                    "parallelism": f"replicas x{world}"},
         "query_heads_per_s": world * w.batch * w.n_heads / t_step,
         "frac_of_nominal_8TBs": per_call / NOMINAL_HBM_GBS,

@@ -49,7 +49,7 @@ typedef struct CUstream_st *dattn_stream_t;
 /* Status codes returned by every int-returning entry point. */
 enum dattn_status {
     DATTN_OK = 0,
-    DATTN_ERR_INVALID_ARG = -1, /* null pointer, non-positive size, bad num_splits */
+    DATTN_ERR_INVALID_ARG = -1, /* null pointer, non-positive size, bad count    */
     DATTN_ERR_UNSUPPORTED = -2, /* head_dim not a multiple of 8 or above 256       */
     DATTN_ERR_MISALIGNED = -3,  /* a tensor pointer is not 16-byte aligned          */
     DATTN_ERR_WORKSPACE = -4,   /* workspace missing, misaligned or too small       */
@@ -67,13 +67,18 @@ const char *dattn_status_string(int status);
 const char *dattn_last_error(void);
 
 /*
- * Execution plan of the fused decode for a shape on the current device: how the
- * KV range is split across CTAs.  Filled by dattn_decode_plan(); informational.
+ * Execution plan of the fused decode for a shape on the current device.
+ * Filled by dattn_decode_plan(); informational.
+ *
+ * The decode is "stream-K": the live positions of the whole batch, flattened
+ * over (sequence, head group, position), are cut into `partitions` equal
+ * ranges, one per CTA, so every CTA streams the same number of KV bytes
+ * whatever the mix of sequence lengths.  A sequence whose positions span
+ * several ranges is finished by a merge kernel.
  */
 typedef struct dattn_plan {
-    int num_splits;      /* position ranges per (sequence, head group)           */
-    int split_len;       /* positions per range (the last one may be shorter)    */
-    int heads_per_cta;   /* heads one CTA handles                                */
+    int partitions;      /* CTAs of the decode grid (equal ranges of positions)  */
+    int heads_per_cta;   /* heads one CTA streams per position                   */
     int head_groups;     /* ceil(n_heads / heads_per_cta)                        */
     int stage_positions; /* positions per shared-memory pipeline stage           */
     int stages;          /* pipeline depth                                       */
@@ -81,29 +86,29 @@ typedef struct dattn_plan {
     int smem_bytes;      /* dynamic shared memory per CTA                        */
     int ctas_per_sm;     /* resident CTAs per SM at that shared-memory size      */
     int sm_count;
-    long long ctas;      /* grid size of the split-K kernel                      */
     size_t workspace_bytes;
 } dattn_plan;
 
 /*
  * Plan the fused decode for (batch, n_heads, head_dim, seq_len) on the current
- * device.  num_splits = 0 lets the library choose (a cost model over the SM
- * count, keyed on seq_len x batch x n_heads); a positive value forces that many
- * position ranges per sequence (clamped to seq_len and to 16384).
+ * device.  num_partitions = 0 lets the library choose (every resident CTA slot
+ * of the GPU, fewer when the batch's capacity is small); a positive value
+ * forces that many partitions (clamped to 65535).
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA (device query failed).
  */
-int dattn_decode_plan(int batch, int n_heads, int head_dim, int seq_len, int num_splits,
+int dattn_decode_plan(int batch, int n_heads, int head_dim, int seq_len, int num_partitions,
                       dattn_plan *plan);
 
 /*
- * Workspace that dattn_decode_f16_ex needs for this shape and num_splits on the
- * current device, in bytes (0 when a single range covers every sequence).
- * The workspace holds fp32 partial softmax states (m, l, acc[head_dim]) per
- * (sequence, head, range); it is scratch, rewritten by every call.
+ * Workspace that dattn_decode_f16_ex needs for this shape and num_partitions
+ * on the current device, in bytes (0 when there is a single partition).  It
+ * holds the batch's live-length prefix sums and one fp32 partial softmax state
+ * (m, l, acc[head_dim]) per head for each (partition, head group) piece; it is
+ * scratch, rewritten by every call.
  * Errors: as dattn_decode_plan, plus INVALID_ARG for a null `bytes`.
  */
 int dattn_decode_workspace_bytes(int batch, int n_heads, int head_dim, int seq_len,
-                                 int num_splits, size_t *bytes);
+                                 int num_partitions, size_t *bytes);
 
 /*
  * Fused decode attention with a caller-provided workspace.
@@ -113,17 +118,18 @@ int dattn_decode_workspace_bytes(int batch, int n_heads, int head_dim, int seq_l
  *   V_cache      [batch, seq_len, n_heads, head_dim]   f16, device
  *   out          [batch, n_heads, head_dim]            f16, device (written)
  *   current_pos  [batch]                               uint32, device
- *   workspace    device scratch, 16-byte aligned, >= dattn_decode_workspace_bytes
- *                (may be NULL when that is 0)
- *   num_splits   0 = library heuristic, > 0 forces the split count
+ *   workspace       device scratch, 16-byte aligned, >= dattn_decode_workspace_bytes
+ *                   (may be NULL when that is 0)
+ *   num_partitions  0 = library choice, > 0 forces the number of partitions
  *
  * For each sequence b and head h, with L = min(current_pos[b], seq_len-1) + 1:
  *   out[b,h,:] = sum_{p<L} softmax_p(Q[b,h,:].K[b,p,h,:] / sqrt(head_dim)) V[b,p,h,:]
  * computed with fp32 accumulation and an online (running max/sum) softmax, then
  * rounded to f16 (round to nearest even).  Positions p >= L are never read: the
- * page's -infinity score gives them weight exactly zero.  The KV range of each
- * sequence is split across CTAs and the partial softmax states are merged by a
- * second kernel (log-sum-exp merge), both enqueued on `stream`.
+ * page's -infinity score gives them weight exactly zero.  The live positions are
+ * divided into equal ranges across CTAs (see dattn_plan); the partial softmax
+ * states of a sequence that spans several ranges are merged by a second kernel
+ * (log-sum-exp merge); both are enqueued on `stream`.
  *
  * Concurrent calls on different streams need different workspaces.
  * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA.
@@ -131,11 +137,11 @@ int dattn_decode_workspace_bytes(int batch, int n_heads, int head_dim, int seq_l
 int dattn_decode_f16_ex(const void *Q, const void *K_cache, const void *V_cache, void *out,
                         int batch, int n_heads, int head_dim, int seq_len,
                         const uint32_t *current_pos, void *workspace, size_t workspace_bytes,
-                        int num_splits, dattn_stream_t stream);
+                        int num_partitions, dattn_stream_t stream);
 
 /*
  * Fused decode attention with the library's own workspace: same operation and
- * arguments as dattn_decode_f16_ex with num_splits = 0.  The workspace is owned
+ * arguments as dattn_decode_f16_ex with num_partitions = 0.  The workspace is owned
  * by the library, one per (device, stream), grown on demand with cudaMalloc
  * (serialised by a mutex) and kept until process exit; a call that has to grow
  * it synchronises the device first.  Make the first call for the largest shape
@@ -182,11 +188,11 @@ int dattn_pv_f16(const void *scores, const void *V_cache, void *out, int batch, 
  * decode time (a runtime that owns all device memory through its own pool, or
  * code that runs where an allocation is forbidden or would synchronise).
  *
- * Same operation and arguments as dattn_decode_f16 (library-chosen split
+ * Same operation and arguments as dattn_decode_f16 (library-chosen partition
  * count).  Instead of a workspace it uses a static device array of
  * DATTN_NOALLOC_SCRATCH_BYTES (32 MiB) that belongs to the library image: every
  * GPU on which the library's code is loaded holds that array until the process
- * exits.  Shapes whose split-K partial states need more than that are rejected
+ * exits.  Shapes whose partial softmax states need more than that are rejected
  * with DATTN_ERR_WORKSPACE before anything is launched; dattn_decode_f16_ex
  * with a caller workspace handles them.
  *

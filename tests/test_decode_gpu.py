@@ -28,13 +28,13 @@ def _built():
     assert dattn.dattn_device_error(clear=True) == 0, "a kernel recorded a pipeline timeout"
 
 
-def run_case(B, H, D, S, cp, seed, num_splits=0, scale=1.0):
+def run_case(B, H, D, S, cp, seed, num_partitions=0, scale=1.0):
     g = torch.Generator(device="cuda").manual_seed(seed)
     q = rand_f16(g, (B, H, D), scale=scale)
     k = rand_f16(g, (B, S, H, D), scale=scale)
     v = rand_f16(g, (B, S, H, D))
     cpt = cur_pos_tensor(cp)
-    out = dattn.decode(q, k, v, cpt, num_splits=num_splits)
+    out = dattn.decode(q, k, v, cpt, num_partitions=num_partitions)
     torch.cuda.synchronize()
     ref = oracle.decode_f64(to_np(q), to_np(k), to_np(v), np.asarray(cp, np.uint32))
     return q, k, v, cpt, out, ref
@@ -68,16 +68,35 @@ def test_decode_matches_oracle(B, H, D, S, cp):
     assert_decode_close(out, ref, f"B={B} H={H} D={D} S={S}")
 
 
-@pytest.mark.parametrize("num_splits", [1, 2, 3, 7, 64, 10_000])
-def test_forced_split_counts_agree(num_splits):
+@pytest.mark.parametrize("num_partitions", [1, 2, 3, 7, 64, 10_000])
+def test_forced_split_counts_agree(num_partitions):
     B, H, D, S, cp = 3, 32, 128, 1200, [1199, 333, 0]
-    *_, out, ref = run_case(B, H, D, S, cp, seed=99, num_splits=num_splits)
-    assert_decode_close(out, ref, f"num_splits={num_splits}")
-    base = run_case(B, H, D, S, cp, seed=99, num_splits=1)[4]
+    *_, out, ref = run_case(B, H, D, S, cp, seed=99, num_partitions=num_partitions)
+    assert_decode_close(out, ref, f"num_partitions={num_partitions}")
+    base = run_case(B, H, D, S, cp, seed=99, num_partitions=1)[4]
     # any two split counts differ only by fp32 rounding order: at most one f16 step
     diff = (out.float() - base.float()).abs()
     ulp = torch.clamp(base.float().abs(), min=2.0**-14) * 2.0**-10
     assert bool((diff <= ulp * 1.01).all())
+
+
+PIECE_SHAPES = [
+    (5, 8, 64, 300, [299, 0, 150, 17, 260]),       # several lane groups per head
+    (3, 64, 256, 100, [99, 5, 50]),                # two head groups per sequence
+    (6, 40, 128, 200, [199, 3, 77, 150, 0, 120]),  # two heads per lane group
+    (40, 4, 32, 30, list(range(0, 40))),           # many short units per partition
+]
+
+
+@pytest.mark.parametrize("partitions", [1, 3, 13, 100])
+@pytest.mark.parametrize("B,H,D,S,cp", PIECE_SHAPES,
+                         ids=[f"B{s[0]}H{s[1]}D{s[2]}S{s[3]}" for s in PIECE_SHAPES])
+def test_partitions_cut_units_anywhere(B, H, D, S, cp, partitions):
+    # ranges that start and end inside units, span several units, or hold
+    # nothing at all, all merge to the same result
+    *_, out, ref = run_case(B, H, D, S, cp, seed=B + H + D + S + partitions,
+                            num_partitions=partitions)
+    assert_decode_close(out, ref, f"partitions={partitions}")
 
 
 def test_large_scores_outlier_channels():
@@ -100,9 +119,9 @@ def test_single_live_position_is_v0_bit_exact():
     g = torch.Generator(device="cuda").manual_seed(3)
     q, k, v = rand_f16(g, (B, H, D), scale=4.0), rand_f16(g, (B, S, H, D)), rand_f16(g, (B, S, H, D))
     for ns in (0, 1, 5):
-        out = dattn.decode(q, k, v, cur_pos_tensor([0] * B), num_splits=ns)
+        out = dattn.decode(q, k, v, cur_pos_tensor([0] * B), num_partitions=ns)
         torch.cuda.synchronize()
-        assert torch.equal(out, v[:, 0]), f"num_splits={ns}"
+        assert torch.equal(out, v[:, 0]), f"num_partitions={ns}"
 
 
 def test_zero_query_gives_mean_of_live_v():
@@ -125,15 +144,15 @@ def test_masked_positions_are_never_read(poison):
     q, k, v = rand_f16(g, (B, H, D)), rand_f16(g, (B, S, H, D)), rand_f16(g, (B, S, H, D))
     cpt = cur_pos_tensor(cp)
     for ns in (0, 1, 9):
-        base = dattn.decode(q, k, v, cpt, num_splits=ns).clone()
+        base = dattn.decode(q, k, v, cpt, num_partitions=ns).clone()
         k2, v2 = k.clone(), v.clone()
         fill = {"nan": float("nan"), "inf": float("inf"), "huge": 60000.0}[poison]
         for b in range(B):
             k2[b, cp[b] + 1:] = fill
             v2[b, cp[b] + 1:] = fill
-        out = dattn.decode(q, k2, v2, cpt, num_splits=ns)
+        out = dattn.decode(q, k2, v2, cpt, num_partitions=ns)
         torch.cuda.synchronize()
-        assert torch.equal(out.view(torch.int16), base.view(torch.int16)), f"num_splits={ns}"
+        assert torch.equal(out.view(torch.int16), base.view(torch.int16)), f"num_partitions={ns}"
 
 
 def test_current_pos_beyond_seq_len_masks_nothing():

@@ -79,9 +79,9 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point(lib):
 
 
 def test_shape_beyond_static_scratch_is_rejected(lib):
-    # 256 sequences x 40 heads x 8192 positions needs ~100 MB of partial
-    # states; the call must fail on the host before launching anything
-    B, H, D, S = 256, 40, 128, 8192
+    # 4096 short sequences x 64 heads need ~140 MB of partial states; the call
+    # must fail on the host before launching anything
+    B, H, D, S = 4096, 64, 128, 16
     need = _native.dattn_decode_workspace_bytes(B, H, D, S, 0)
     assert need > SCRATCH_BYTES  # guarantees the host-side rejection below
     fake = 1 << 20  # aligned, never dereferenced: nothing is launched on rejection

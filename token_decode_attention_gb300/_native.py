@@ -27,12 +27,11 @@ class DattnError(RuntimeError):
 
 
 class Plan(ctypes.Structure):
-    _fields_ = [("num_splits", ctypes.c_int), ("split_len", ctypes.c_int),
-                ("heads_per_cta", ctypes.c_int), ("head_groups", ctypes.c_int),
-                ("stage_positions", ctypes.c_int), ("stages", ctypes.c_int),
-                ("threads_per_cta", ctypes.c_int), ("smem_bytes", ctypes.c_int),
-                ("ctas_per_sm", ctypes.c_int), ("sm_count", ctypes.c_int),
-                ("ctas", ctypes.c_longlong), ("workspace_bytes", ctypes.c_size_t)]
+    _fields_ = [("partitions", ctypes.c_int), ("heads_per_cta", ctypes.c_int),
+                ("head_groups", ctypes.c_int), ("stage_positions", ctypes.c_int),
+                ("stages", ctypes.c_int), ("threads_per_cta", ctypes.c_int),
+                ("smem_bytes", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
+                ("sm_count", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -134,23 +133,23 @@ def dattn_version() -> int:
 
 
 def dattn_decode_plan(batch: int, n_heads: int, head_dim: int, seq_len: int,
-                      num_splits: int = 0) -> dict:
+                      num_partitions: int = 0) -> dict:
     plan = Plan()
-    _check(load().dattn_decode_plan(batch, n_heads, head_dim, seq_len, num_splits,
+    _check(load().dattn_decode_plan(batch, n_heads, head_dim, seq_len, num_partitions,
                                     ctypes.byref(plan)), "dattn_decode_plan")
     return plan.as_dict()
 
 
 def dattn_decode_workspace_bytes(batch: int, n_heads: int, head_dim: int, seq_len: int,
-                                 num_splits: int = 0) -> int:
+                                 num_partitions: int = 0) -> int:
     n = ctypes.c_size_t(0)
-    _check(load().dattn_decode_workspace_bytes(batch, n_heads, head_dim, seq_len, num_splits,
+    _check(load().dattn_decode_workspace_bytes(batch, n_heads, head_dim, seq_len, num_partitions,
                                                ctypes.byref(n)),
            "dattn_decode_workspace_bytes")
     return int(n.value)
 
 
-def dattn_decode_f16_ex(q, k, v, out, current_pos, workspace=None, num_splits: int = 0,
+def dattn_decode_f16_ex(q, k, v, out, current_pos, workspace=None, num_partitions: int = 0,
                         stream=None) -> None:
     B, H, D, S = _qkv_dims(q, k)
     args = (_tensor(q, "Q", (B, H, D)), _tensor(k, "K_cache", (B, S, H, D)),
@@ -160,7 +159,7 @@ def dattn_decode_f16_ex(q, k, v, out, current_pos, workspace=None, num_splits: i
         ws_ptr = _tensor(workspace, "workspace", None, workspace.dtype)
         ws_bytes = workspace.numel() * workspace.element_size()
     _check(load().dattn_decode_f16_ex(*args, B, H, D, S, _cur_pos(current_pos, B), ws_ptr,
-                                      ws_bytes, num_splits, _stream_handle(stream)),
+                                      ws_bytes, num_partitions, _stream_handle(stream)),
            "dattn_decode_f16_ex")
 
 
@@ -204,15 +203,15 @@ def dattn_device_error(clear: bool = True) -> int:
 
 # ------------------------------------------------------- convenience forms
 
-def decode(q, k, v, current_pos, num_splits: int = 0, out=None, workspace=None, stream=None):
+def decode(q, k, v, current_pos, num_partitions: int = 0, out=None, workspace=None, stream=None):
     """Fused decode attention; allocates ``out`` and the workspace with torch if not given."""
     B, H, D, S = _qkv_dims(q, k)
     if out is None:
         out = torch.empty((B, H, D), dtype=torch.float16, device=q.device)
     if workspace is None:
-        n = dattn_decode_workspace_bytes(B, H, D, S, num_splits)
+        n = dattn_decode_workspace_bytes(B, H, D, S, num_partitions)
         workspace = torch.empty((max(n, 16),), dtype=torch.uint8, device=q.device)
-    dattn_decode_f16_ex(q, k, v, out, current_pos, workspace, num_splits, stream)
+    dattn_decode_f16_ex(q, k, v, out, current_pos, workspace, num_partitions, stream)
     return out
 
 

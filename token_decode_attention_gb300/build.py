@@ -18,9 +18,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdattn.so")
-SOURCES = ["decode_splitk.cu", "combine.cu", "split_calls.cu", "decode_noalloc.cu",
+SOURCES = ["decode_streamk.cu", "combine.cu", "split_calls.cu", "decode_noalloc.cu",
            "dattn_api.cpp"]
-HEADERS = ["dattn_internal.h", "ptx.cuh"]
+HEADERS = ["dattn_internal.h", "ptx.cuh", "streamk.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

@@ -1,18 +1,20 @@
-// combine.cu -- merge of the split-K partial softmax states into the f16 output.
+// combine.cu -- merge of the stream-K partial softmax states into f16 output.
 //
-// Each position range j of a sequence leaves (m_j, l_j, acc_j[D]) with
-//   m_j = max score of the range (log2 units), l_j = sum 2^(s - m_j),
-//   acc_j = sum 2^(s - m_j) V.
-// The exact softmax-weighted sum over the whole live range is
+// A unit (sequence b, head group g) whose live positions span several
+// partitions c_first..c_last was processed in pieces; each piece j left
+//   m_j = max score (log2 units), l_j = sum 2^(s - m_j), acc_j = sum 2^(s - m_j) V
+// per head in workspace slot piece_slot(j, u) (see streamk.h).  The exact
+// softmax-weighted sum over the unit's whole live range is
 //   out = sum_j 2^(m_j - M) acc_j / sum_j 2^(m_j - M) l_j,   M = max_j m_j,
 // the log-sum-exp merge of a max-subtracted softmax (exact in real arithmetic).
-// Ranges at or past the live length were never written and are not read; a
-// sequence whose live length fits one range already has its output written by
-// the split-K kernel and is skipped here.
+// Units held by a single partition already have their output written by the
+// decode kernel and are skipped.
 //
-// One CTA per (sequence, head).  Launched with programmatic dependent launch:
-// the CTAs may start while the split-K kernel drains, and wait for its memory
-// with griddepcontrol.wait before reading the workspace.
+// Grid: one CTA per (sequence, head, chunk of 32 channels), so even a single
+// long sequence spreads its merge over H * D/32 CTAs; inside a CTA, threads
+// take (piece, float4) pairs and keep several loads in flight.  Launched with
+// programmatic dependent launch: it may start while the decode kernel drains
+// and waits on griddepcontrol.wait before touching the workspace.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -20,111 +22,145 @@
 
 #include "dattn_internal.h"
 #include "ptx.cuh"
+#include "streamk.h"
 
 namespace dattn {
 namespace {
 
-constexpr int kCombineThreads = 256;
-constexpr int kCombineWarps = kCombineThreads / 32;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kChunk = 32;  // channels per CTA
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineArgs a) {
-    pdl_wait_primary();
-    extern __shared__ __align__(16) float csm[];
-    float *red = csm;                        // [kCombineWarps]
-    float *part = csm + 32;                  // [kCombineWarps][D]
-    float *wts = part + kCombineWarps * a.D; // [num_splits]
+__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) {
+    __shared__ float red[kWarps];
+    __shared__ float4 part[kThreads];
 
-    const long long bh = blockIdx.x;
+    const int nchunks = (a.D + kChunk - 1) / kChunk;
+    const long long idx = blockIdx.x;
+    const int chunk = static_cast<int>(idx % nchunks);
+    const long long bh = idx / nchunks;
+    const int h = static_cast<int>(bh % a.H);
     const long long b = bh / a.H;
-    const uint32_t cp = a.cur_pos[b];
-    const int L = cp >= static_cast<uint32_t>(a.S - 1) ? a.S : static_cast<int>(cp) + 1;
-    const int nsl = (L + a.split_len - 1) / a.split_len;
-    if (nsl <= 1) return;
+    const int g = h / a.heads_per_cta;
+    const int hl = h - g * a.heads_per_cta;
+    const long long u = b * a.head_groups + g;
+
+    const uint32_t cp = __ldg(a.cur_pos + b);
+    const long long Lb = cp >= static_cast<uint32_t>(a.S - 1) ? a.S : static_cast<long long>(cp) + 1;
+
+    pdl_wait_primary();  // the decode kernel's workspace writes are visible after this
+    const long long nhg = a.head_groups;
+    const long long W = nhg * a.ws_prefix[a.B];
+    const long long Pu = nhg * a.ws_prefix[b] + g * Lb;
+    const long long c_first = range_owner(Pu, W, a.partitions);
+    const long long c_last = range_owner(Pu + Lb - 1, W, a.partitions);
+    if (c_first == c_last) return;  // written whole by the decode kernel
+    const int npieces = static_cast<int>(c_last - c_first + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const float2 *ml = a.ws_ml + bh * a.num_splits;
+    const size_t hg_stride = a.heads_per_cta;
+    auto ml_of = [&](int j) -> float2 {
+        return a.ws_ml[static_cast<size_t>(piece_slot(c_first + j, u)) * hg_stride + hl];
+    };
 
     float M = -INFINITY;
-    for (int j = tid; j < nsl; j += kCombineThreads) M = fmaxf(M, ml[j].x);
-    M = warp_max(M);
+    for (int j = tid; j < npieces; j += kThreads) M = fmaxf(M, ml_of(j).x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     if (lane == 0) red[warp] = M;
     __syncthreads();
     M = red[0];
-    for (int w = 1; w < kCombineWarps; ++w) M = fmaxf(M, red[w]);
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, red[w]);
     __syncthreads();
 
     float lsum = 0.f;
-    for (int j = tid; j < nsl; j += kCombineThreads) {
-        const float2 v = ml[j];
-        const float w = exp2f(v.x - M);
-        wts[j] = w;
-        lsum = fmaf(w, v.y, lsum);
+    for (int j = tid; j < npieces; j += kThreads) {
+        const float2 v = ml_of(j);
+        lsum = fmaf(fast_exp2(v.x - M), v.y, lsum);
     }
-    lsum = warp_sum(lsum);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
     if (lane == 0) red[warp] = lsum;
     __syncthreads();
     lsum = 0.f;
-    for (int w = 0; w < kCombineWarps; ++w) lsum += red[w];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) lsum += red[w];
 
-    // Weighted sum of the partial accumulators: warp w takes ranges j = w mod 8,
-    // each lane four consecutive channels (two chunks when D > 128).
-    const int D = a.D;
-    const int D4 = D / 4;
-    const float *accb = a.ws_acc + bh * a.num_splits * D;
-    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
-    for (int j = warp; j < nsl; j += kCombineWarps) {
-        const float w = wts[j];
-        const float4 *row = reinterpret_cast<const float4 *>(accb + static_cast<size_t>(j) * D);
-        if (lane < D4) {
-            const float4 v = row[lane];
-            s0.x = fmaf(w, v.x, s0.x); s0.y = fmaf(w, v.y, s0.y);
-            s0.z = fmaf(w, v.z, s0.z); s0.w = fmaf(w, v.w, s0.w);
+    // weighted sum of the partial accumulators for this chunk of channels
+    const int c0 = chunk * kChunk;
+    const int width = min(kChunk, a.D - c0);  // a multiple of 8
+    const int f4 = width / 4;                 // float4 per piece row
+    const int nsub = kThreads / f4;           // pieces in flight per pass
+    const int sub = tid / f4, f = tid - sub * f4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (sub < nsub) {
+        int j = sub;
+        for (; j + 3 * nsub < npieces; j += 4 * nsub) {
+            float4 v[4];
+            float w[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int jj = j + r * nsub;
+                const size_t row = static_cast<size_t>(piece_slot(c_first + jj, u)) * hg_stride + hl;
+                v[r] = *reinterpret_cast<const float4 *>(a.ws_acc + row * a.D + c0 + f * 4);
+                w[r] = fast_exp2(a.ws_ml[row].x - M);
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                acc.x = fmaf(w[r], v[r].x, acc.x);
+                acc.y = fmaf(w[r], v[r].y, acc.y);
+                acc.z = fmaf(w[r], v[r].z, acc.z);
+                acc.w = fmaf(w[r], v[r].w, acc.w);
+            }
         }
-        if (lane + 32 < D4) {
-            const float4 v = row[lane + 32];
-            s1.x = fmaf(w, v.x, s1.x); s1.y = fmaf(w, v.y, s1.y);
-            s1.z = fmaf(w, v.z, s1.z); s1.w = fmaf(w, v.w, s1.w);
+        for (; j < npieces; j += nsub) {
+            const size_t row = static_cast<size_t>(piece_slot(c_first + j, u)) * hg_stride + hl;
+            const float4 v = *reinterpret_cast<const float4 *>(a.ws_acc + row * a.D + c0 + f * 4);
+            const float w = fast_exp2(a.ws_ml[row].x - M);
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
         }
     }
-    if (lane < D4) reinterpret_cast<float4 *>(part + warp * D)[lane] = s0;
-    if (lane + 32 < D4) reinterpret_cast<float4 *>(part + warp * D)[lane + 32] = s1;
+    part[tid] = acc;
     __syncthreads();
-    for (int d = tid; d < D; d += kCombineThreads) {
-        float num = 0.f;
-        for (int w = 0; w < kCombineWarps; ++w) num += part[w * D + d];
-        reinterpret_cast<__half *>(a.out)[bh * D + d] = __float2half_rn(num / lsum);
+    if (tid < f4) {
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < nsub; ++r) {
+            const float4 v = part[r * f4 + tid];
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+        const float inv = 1.f / lsum;
+        __half2 lo = __floats2half2_rn(s.x * inv, s.y * inv);
+        __half2 hi = __floats2half2_rn(s.z * inv, s.w * inv);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t *>(&lo);
+        packed.y = *reinterpret_cast<uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(reinterpret_cast<__half *>(a.out) + bh * a.D + c0 + tid * 4) =
+            packed;
     }
 }
 
 }  // namespace
 
-size_t combine_smem_bytes(int num_splits, int D) {
-    return sizeof(float) * (32 + static_cast<size_t>(kCombineWarps) * D + num_splits);
-}
-
-cudaError_t combine_configure_smem(int max_smem) {
-    return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                max_smem);
-}
-
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream) {
-    const long long blocks = static_cast<long long>(a.B) * a.H;
+    const long long blocks = static_cast<long long>(a.B) * a.H * ((a.D + kChunk - 1) / kChunk);
     if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-    cfg.blockDim = dim3(kCombineThreads);
-    cfg.dynamicSmemBytes = combine_smem_bytes(a.num_splits, a.D);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

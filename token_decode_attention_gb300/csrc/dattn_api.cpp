@@ -1,10 +1,10 @@
 // dattn_api.cpp -- the C ABI declared in include/dattn.h.
 //
 // Host side of the library: argument validation (before anything is
-// launched), the split-K plan (a small cost model over the SM count), the
+// launched), the stream-K plan (tiling, pipeline depth, partition count), the
 // library-owned workspace of dattn_decode_f16, status codes and per-thread
 // error messages.  The arithmetic of the operation runs only in the CUDA
-// kernels (decode_splitk.cu, combine.cu, split_calls.cu).
+// kernels (decode_streamk.cu, combine.cu, split_calls.cu).
 #include "dattn.h"
 
 #include <cuda_runtime.h>
@@ -27,15 +27,15 @@ namespace {
 using dattn::DecodeVariant;
 
 constexpr int kVersion = 10000;        // 1.0.0
-constexpr int kMaxSplits = 16384;      // position ranges per sequence
+constexpr int kMaxPartitions = 65535;  // CTAs of the decode grid
+constexpr long long kMinPositions = 16;  // positions per partition chosen by the library
 constexpr int kMaxHeadDim = 256;
 constexpr int kMaxHeadsPerLaneGroup = 4;  // register slots per lane group (KMAX)
 constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
 constexpr int kStageTargetBytes = 32 * 1024;
-constexpr int kTwoPerSmBudget = 110 * 1024;
-constexpr double kModelBandwidth = 6.5e12;  // bytes/s used by the split cost model
-constexpr double kCtaOverheadS = 1.5e-6;    // pipeline fill per CTA wave
-constexpr double kCombineLaunchS = 2.0e-6;
+constexpr int kTwoPerSmBudget = 110 * 1024;  // ring bytes per CTA at 2 CTAs/SM
+constexpr int kOnePerSmBudget = 200 * 1024;  // ring bytes per CTA at 1 CTA/SM
+constexpr int kMaxStages = 12;
 
 thread_local std::string g_last_error;
 
@@ -87,9 +87,7 @@ int device_info(DeviceInfo *out) {
     e = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute(smem opt-in)");
     e = dattn::decode_configure_smem(di.max_smem_optin);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(split-K kernel)");
-    e = dattn::combine_configure_smem(di.max_smem_optin);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(combine kernel)");
+    if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(decode kernel)");
     e = dattn::device_error_word(&di.err_word);
     if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(error word)");
     g_devices[dev] = di;
@@ -101,10 +99,9 @@ int device_info(DeviceInfo *out) {
 
 struct Plan {
     DecodeVariant v{};
-    int HG = 0, NHG = 0, PHI = 0, P = 0, NST = 0, NS = 0, chunk = 0;
-    int smem = 0, bar_offset = 0, ctas_per_sm = 0, sms = 0;
-    long long ctas = 0;
-    size_t ws_acc_bytes = 0, ws_bytes = 0;
+    int HG = 0, NHG = 0, PHI = 0, P = 0, NST = 0, G = 0;
+    int smem = 0, merge_offset = 0, bar_offset = 0, ctas_per_sm = 0, sms = 0;
+    size_t prefix_bytes = 0, acc_bytes = 0, ws_bytes = 0;
 };
 
 int next_pow2(int x) {
@@ -114,6 +111,7 @@ int next_pow2(int x) {
 }
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
+static size_t round_up_sz(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
 int validate_dims(int B, int H, int D, int S) {
     if (B <= 0 || H <= 0 || D <= 0 || S <= 0)
@@ -134,46 +132,27 @@ using PlanKey = std::tuple<int, int, int, int, int, int>;
 std::mutex g_plan_mutex;
 std::map<PlanKey, Plan> g_plans;
 
-// Choose the number of position ranges per sequence: the smallest modelled time
-// over candidate split counts, where a launch costs waves x (range bytes over
-// one CTA slot's share of HBM bandwidth + pipeline fill), plus the combine
-// kernel and its workspace traffic when there is more than one range.
-int choose_splits(const Plan &p, int B, int H, int D, int S) {
+// Number of partitions (CTAs) when the caller leaves it to the library: every
+// resident CTA slot of the GPU, unless the batch's capacity is so small that a
+// partition would hold fewer than kMinPositions positions (then fewer CTAs, to
+// keep the partial states the combine must merge few).
+int choose_partitions(const Plan &p, int B, int S) {
     const long long slots = static_cast<long long>(p.sms) * p.ctas_per_sm;
-    const double slot_bw = kModelBandwidth / static_cast<double>(slots);
-    const double bytes_pos = static_cast<double>(p.HG) * D * 4.0;
-    const long long units = static_cast<long long>(B) * p.NHG;
-    const int ns_max = static_cast<int>(std::min<long long>({S, kMaxSplits, 8 * slots}));
-    int best = 1;
-    double best_t = INFINITY;
-    for (int ns = 1; ns <= ns_max; ++ns) {
-        const int chunk = (S + ns - 1) / ns;
-        if (ns > 1 && chunk < p.P) break;  // every range holds at least one full stage
-        const int nse = (S + chunk - 1) / chunk;
-        if (nse != ns) continue;
-        const long long ctas = units * nse;
-        const double waves = std::ceil(static_cast<double>(ctas) / static_cast<double>(slots));
-        double t = waves * (chunk * bytes_pos / slot_bw + kCtaOverheadS);
-        if (nse > 1)
-            t += kCombineLaunchS +
-                 static_cast<double>(B) * H * nse * (D + 2) * 4.0 * 2.0 / kModelBandwidth;
-        if (t < best_t * (1.0 - 1e-9)) {
-            best_t = t;
-            best = nse;
-        }
-    }
-    return best;
+    const long long capacity = static_cast<long long>(B) * p.NHG * S;
+    const long long min_pos = std::max<long long>(kMinPositions, 2LL * p.P);
+    const long long by_work = std::max<long long>(1, capacity / min_pos);
+    return static_cast<int>(std::min<long long>({slots, by_work, kMaxPartitions}));
 }
 
-int make_plan(int B, int H, int D, int S, int num_splits, Plan *out) {
+int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
     if (int st = validate_dims(B, H, D, S)) return st;
-    if (num_splits < 0)
-        return fail(DATTN_ERR_INVALID_ARG, "num_splits=%d must be >= 0", num_splits);
+    if (num_partitions < 0)
+        return fail(DATTN_ERR_INVALID_ARG, "num_partitions=%d must be >= 0", num_partitions);
     DeviceInfo di;
     if (int st = device_info(&di)) return st;
     int dev = 0;
     if (int st = current_device(&dev)) return st;
-    const PlanKey key{dev, B, H, D, S, num_splits};
+    const PlanKey key{dev, B, H, D, S, num_partitions};
     {
         std::lock_guard<std::mutex> lock(g_plan_mutex);
         auto it = g_plans.find(key);
@@ -184,25 +163,41 @@ int make_plan(int B, int H, int D, int S, int num_splits, Plan *out) {
     }
     Plan p;
     p.sms = di.sms;
-    const int bdx = std::min(32, next_pow2(D / 8));
-    const int bdy = 32 / bdx;
-    const int nlg = dattn::kConsumerWarps * bdy;
-    int hg_max = std::min(nlg * kMaxHeadsPerLaneGroup, std::max(1, kMaxRowBytesKV / (D * 4)));
+    // lanes per KV row and 8-element chunks per lane
+    const int c8 = D / 8;
+    int bdx, ch;
+    if (c8 <= 8) {
+        bdx = next_pow2(c8);
+        ch = 1;
+    } else if (c8 <= 16) {
+        bdx = 8;
+        ch = 2;
+    } else {
+        bdx = 16;
+        ch = 2;
+    }
+    const int nlg = dattn::kConsumerWarps * (32 / bdx);  // lane groups per CTA
+    const int kmax_cap = ch == 2 ? 2 : 4;
+    const int hg_max = std::min(nlg * kmax_cap, std::max(1, kMaxRowBytesKV / (D * 4)));
     p.NHG = (H + hg_max - 1) / hg_max;
     p.HG = (H + p.NHG - 1) / p.NHG;
     p.PHI = p.HG >= nlg ? 1 : std::min(32, nlg / p.HG);
     const int kmax = (p.HG * p.PHI + nlg - 1) / nlg;
-    p.v = DecodeVariant{bdx, kmax};
+    p.v = DecodeVariant{bdx, ch, kmax};
     const int row_bytes = p.HG * D * 2;
     int P = std::max(1, std::min(256, kStageTargetBytes / 2 / row_bytes));
     P = std::max(p.PHI, P / p.PHI * p.PHI);
     p.P = P;
     const int stage_bytes = 2 * P * row_bytes;
-    const int merge_bytes = p.HG * p.PHI * (D + 2) * 4;
-    int nst = kTwoPerSmBudget / stage_bytes;
-    if (nst < 2) nst = (di.max_smem_optin - 1024) / stage_bytes;
-    p.NST = std::max(2, std::min(8, nst));
-    p.bar_offset = round_up(std::max(p.NST * stage_bytes, merge_bytes), 128);
+    const int merge_bytes = p.PHI > 1 ? p.HG * p.PHI * (D + 2) * 4 : 0;
+    const int ring_budget = dattn::decode_min_blocks(ch, kmax) == 2
+                                ? kTwoPerSmBudget - merge_bytes
+                                : kOnePerSmBudget - merge_bytes;
+    int nst = ring_budget / stage_bytes;
+    if (nst < 2) nst = (di.max_smem_optin - 1024 - merge_bytes) / stage_bytes;
+    p.NST = std::max(2, std::min(kMaxStages, nst));
+    p.merge_offset = p.NST * stage_bytes;
+    p.bar_offset = round_up(p.merge_offset + merge_bytes, 16);
     p.smem = p.bar_offset + p.NST * 16 + 16;
     if (p.smem > di.max_smem_optin)
         return fail(DATTN_ERR_UNSUPPORTED, "shape needs %d B of shared memory (limit %d)",
@@ -210,20 +205,20 @@ int make_plan(int B, int H, int D, int S, int num_splits, Plan *out) {
     cudaError_t e = dattn::decode_occupancy(p.v, p.smem, &p.ctas_per_sm);
     if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
     if (p.ctas_per_sm < 1)
-        return fail(DATTN_ERR_UNSUPPORTED, "split-K kernel does not fit on an SM");
-    int ns = num_splits > 0 ? std::min({num_splits, S, kMaxSplits})
-                            : choose_splits(p, B, H, D, S);
-    p.chunk = (S + ns - 1) / ns;
-    p.NS = (S + p.chunk - 1) / p.chunk;
-    p.ctas = static_cast<long long>(B) * p.NHG * p.NS;
-    if (p.ctas > 0x7fffffffLL)
-        return fail(DATTN_ERR_UNSUPPORTED, "grid of %lld CTAs is too large", p.ctas);
-    if (p.NS > 1) {
-        const size_t rows = static_cast<size_t>(B) * H * p.NS;
-        p.ws_acc_bytes = (rows * D * sizeof(float) + 255) / 256 * 256;
-        p.ws_bytes = p.ws_acc_bytes + rows * sizeof(float2);
-        if (dattn::combine_smem_bytes(p.NS, D) > static_cast<size_t>(di.max_smem_optin))
-            return fail(DATTN_ERR_UNSUPPORTED, "num_splits=%d too large for the combine", p.NS);
+        return fail(DATTN_ERR_UNSUPPORTED, "decode kernel does not fit on an SM");
+    p.G = num_partitions > 0 ? std::min(num_partitions, kMaxPartitions)
+                             : choose_partitions(p, B, S);
+    // partition arithmetic multiplies a partition index by the flattened
+    // position count: keep it inside 64 bits
+    const double capacity = static_cast<double>(B) * p.NHG * S;
+    if (capacity * (p.G + 1.0) > 4.0e18)
+        return fail(DATTN_ERR_UNSUPPORTED, "batch of %.3g positions is too large", capacity);
+    if (p.G > 1) {
+        const size_t units = static_cast<size_t>(B) * p.NHG;
+        const size_t rows = (static_cast<size_t>(p.G) + units) * p.HG;
+        p.prefix_bytes = round_up_sz((static_cast<size_t>(B) + 1) * sizeof(long long), 256);
+        p.acc_bytes = round_up_sz(rows * D * sizeof(float), 256);
+        p.ws_bytes = p.prefix_bytes + p.acc_bytes + rows * sizeof(float2);
     }
     {
         std::lock_guard<std::mutex> lock(g_plan_mutex);
@@ -251,16 +246,16 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
                   cudaStream_t stream) {
     DeviceInfo di;
     if (int st = device_info(&di)) return st;
+    char *ws = static_cast<char *>(workspace);
     dattn::DecodeArgs a{};
     a.Q = Q;
     a.K = K;
     a.V = V;
     a.out = out;
     a.cur_pos = cur_pos;
-    a.ws_acc = p.NS > 1 ? static_cast<float *>(workspace) : nullptr;
-    a.ws_ml = p.NS > 1
-                  ? reinterpret_cast<float2 *>(static_cast<char *>(workspace) + p.ws_acc_bytes)
-                  : nullptr;
+    a.ws_prefix = p.G > 1 ? reinterpret_cast<long long *>(ws) : nullptr;
+    a.ws_acc = p.G > 1 ? reinterpret_cast<float *>(ws + p.prefix_bytes) : nullptr;
+    a.ws_ml = p.G > 1 ? reinterpret_cast<float2 *>(ws + p.prefix_bytes + p.acc_bytes) : nullptr;
     a.err = di.err_word;
     a.B = B;
     a.H = H;
@@ -271,25 +266,27 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
     a.phases = p.PHI;
     a.stage_pos = p.P;
     a.stages = p.NST;
-    a.num_splits = p.NS;
-    a.split_len = p.chunk;
+    a.partitions = p.G;
+    a.merge_offset = p.merge_offset;
     a.bar_offset = p.bar_offset;
     a.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
-    cudaError_t e = dattn::launch_decode_splitk(a, p.v, p.ctas, p.smem, stream);
+    cudaError_t e = dattn::launch_decode(a, p.v, p.smem, stream);
     if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess) return fail_cuda(e, "split-K kernel launch");
-    if (p.NS > 1) {
+    if (e != cudaSuccess) return fail_cuda(e, "decode kernel launch");
+    if (p.G > 1) {
         dattn::CombineArgs c{};
         c.ws_acc = a.ws_acc;
         c.ws_ml = a.ws_ml;
+        c.ws_prefix = a.ws_prefix;
         c.cur_pos = cur_pos;
         c.out = out;
         c.B = B;
         c.H = H;
         c.D = D;
         c.S = S;
-        c.num_splits = p.NS;
-        c.split_len = p.chunk;
+        c.heads_per_cta = p.HG;
+        c.head_groups = p.NHG;
+        c.partitions = p.G;
         e = dattn::launch_combine(c, stream);
         if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return fail_cuda(e, "combine kernel launch");
@@ -330,13 +327,12 @@ const char *dattn_status_string(int status) {
 
 const char *dattn_last_error(void) { return g_last_error.c_str(); }
 
-int dattn_decode_plan(int batch, int n_heads, int head_dim, int seq_len, int num_splits,
+int dattn_decode_plan(int batch, int n_heads, int head_dim, int seq_len, int num_partitions,
                       dattn_plan *plan) {
     if (plan == nullptr) return fail(DATTN_ERR_INVALID_ARG, "plan is NULL");
     Plan p;
-    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_splits, &p)) return st;
-    plan->num_splits = p.NS;
-    plan->split_len = p.chunk;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, &p)) return st;
+    plan->partitions = p.G;
     plan->heads_per_cta = p.HG;
     plan->head_groups = p.NHG;
     plan->stage_positions = p.P;
@@ -345,16 +341,15 @@ int dattn_decode_plan(int batch, int n_heads, int head_dim, int seq_len, int num
     plan->smem_bytes = p.smem;
     plan->ctas_per_sm = p.ctas_per_sm;
     plan->sm_count = p.sms;
-    plan->ctas = p.ctas;
     plan->workspace_bytes = p.ws_bytes;
     return DATTN_OK;
 }
 
 int dattn_decode_workspace_bytes(int batch, int n_heads, int head_dim, int seq_len,
-                                 int num_splits, size_t *bytes) {
+                                 int num_partitions, size_t *bytes) {
     if (bytes == nullptr) return fail(DATTN_ERR_INVALID_ARG, "bytes is NULL");
     Plan p;
-    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_splits, &p)) return st;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, &p)) return st;
     *bytes = p.ws_bytes;
     return DATTN_OK;
 }
@@ -362,17 +357,17 @@ int dattn_decode_workspace_bytes(int batch, int n_heads, int head_dim, int seq_l
 int dattn_decode_f16_ex(const void *Q, const void *K_cache, const void *V_cache, void *out,
                         int batch, int n_heads, int head_dim, int seq_len,
                         const uint32_t *current_pos, void *workspace, size_t workspace_bytes,
-                        int num_splits, dattn_stream_t stream) {
+                        int num_partitions, dattn_stream_t stream) {
     if (int st = check_tensor(Q, "Q")) return st;
     if (int st = check_tensor(K_cache, "K_cache")) return st;
     if (int st = check_tensor(V_cache, "V_cache")) return st;
     if (int st = check_tensor(out, "out")) return st;
     if (int st = check_cur_pos(current_pos)) return st;
     if (int st = validate_dims(batch, n_heads, head_dim, seq_len)) return st;
-    if (num_splits < 0)
-        return fail(DATTN_ERR_INVALID_ARG, "num_splits=%d must be >= 0", num_splits);
+    if (num_partitions < 0)
+        return fail(DATTN_ERR_INVALID_ARG, "num_partitions=%d must be >= 0", num_partitions);
     Plan p;
-    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_splits, &p)) return st;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, &p)) return st;
     if (p.ws_bytes > 0) {
         if (workspace == nullptr)
             return fail(DATTN_ERR_WORKSPACE, "workspace of %zu bytes required, got NULL",

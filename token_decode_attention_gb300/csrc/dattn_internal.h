@@ -9,8 +9,8 @@
 
 namespace dattn {
 
-// Consumer warps per CTA of the fused split-K kernel; one more warp issues the
-// bulk copies.
+// Consumer warps per CTA of the decode kernel; one more warp issues the bulk
+// copies.
 constexpr int kConsumerWarps = 8;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
 
@@ -19,20 +19,23 @@ constexpr unsigned kErrConsumerWait = 1u;
 constexpr unsigned kErrProducerWait = 2u;
 constexpr unsigned kErrDrainWait = 4u;
 
-// Arguments of the fused split-K decode kernel.
+// Arguments of the stream-K decode kernel.
 //
-// Grid: one CTA per (sequence b, head group g, split j), flattened as
-// ((b * head_groups + g) * num_splits + j).  The CTA owns heads
-// [g*heads_per_cta, min(H, (g+1)*heads_per_cta)) and positions
-// [j*split_len, min((j+1)*split_len, L_b)).
+// Units are (sequence b, head group g), u = b * head_groups + g, each holding
+// the L_b live positions of heads [g*heads_per_cta, min(H, (g+1)*heads_per_cta)).
+// Their positions, flattened unit after unit (W in total), are cut into
+// `partitions` equal ranges, one per CTA (see streamk.h).  A CTA writes the
+// f16 output of every unit it covers entirely and a partial softmax state for
+// the others.
 struct DecodeArgs {
     const void *Q;            // f16 [B,H,D]
     const void *K;            // f16 [B,S,H,D]
     const void *V;            // f16 [B,S,H,D]
     void *out;                // f16 [B,H,D]
     const uint32_t *cur_pos;  // [B]
-    float *ws_acc;            // [B,H,NS,D] unnormalised partial outputs
-    float2 *ws_ml;            // [B,H,NS]   partial (running max in log2 units, sum)
+    long long *ws_prefix;     // [B+1] live positions before each sequence (written by CTA 0)
+    float *ws_acc;            // [(G+U), HG, D] unnormalised partial outputs
+    float2 *ws_ml;            // [(G+U), HG]    partial (running max, log2 units; sum)
     unsigned *err;            // device error word
     int B, H, D, S;
     int heads_per_cta;  // HG
@@ -40,42 +43,44 @@ struct DecodeArgs {
     int phases;         // PHI: lane groups sharing one head interleave positions
     int stage_pos;      // P: positions per pipeline stage (a multiple of PHI)
     int stages;         // NST: pipeline depth
-    int num_splits;     // NS
-    int split_len;      // positions per split
-    int bar_offset;     // byte offset of the mbarriers in dynamic shared memory
-    float qscale;       // log2(e) / sqrt(D), folded into q
+    int partitions;     // G: CTAs
+    int merge_offset;   // byte offset of the phase-merge area in dynamic smem
+    int bar_offset;     // byte offset of the mbarriers in dynamic smem
+    float qscale;       // log2(e) / sqrt(D), applied to each dot product
 };
 
-// Arguments of the combine kernel (log-sum-exp merge of the splits).
+// Arguments of the combine kernel (log-sum-exp merge of the pieces of a unit).
 struct CombineArgs {
     const float *ws_acc;
     const float2 *ws_ml;
+    const long long *ws_prefix;
     const uint32_t *cur_pos;
     void *out;
     int B, H, D, S;
-    int num_splits;
-    int split_len;
+    int heads_per_cta;
+    int head_groups;
+    int partitions;
 };
 
-// Compile-time shape of one fused-kernel instance: lanes per KV row (head_dim/8
-// rounded up to a power of two) and the number of (head, phase) slots each lane
-// group keeps in registers.
+// Compile-time shape of one decode-kernel instance.
 struct DecodeVariant {
-    int bdx;   // 1, 2, 4, 8, 16, 32
-    int kmax;  // 1..4
+    int bdx;   // lanes per KV row: 1, 2, 4, 8 (chunks = 1) or 8, 16 (chunks = 2)
+    int ch;    // 8-element chunks per lane: 1 or 2
+    int kmax;  // (head, phase) slots per lane group: 1..4 (1..2 when ch = 2)
 };
 
-// Launch the fused split-K kernel.  smem = dynamic shared memory bytes.
-cudaError_t launch_decode_splitk(const DecodeArgs &a, DecodeVariant v, long long ctas,
-                                 int smem, cudaStream_t stream);
+// CTAs per SM a variant is compiled for.  Variants that keep three or more
+// 8-channel state blocks per lane are compiled for one CTA per SM, so they get
+// enough registers not to spill, and use a deeper shared-memory ring instead
+// of a second CTA.
+constexpr int decode_min_blocks(int ch, int kmax) { return ch * kmax >= 3 ? 1 : 2; }
+
+// Launch the decode kernel.  smem = dynamic shared memory bytes.
+cudaError_t launch_decode(const DecodeArgs &a, DecodeVariant v, int smem, cudaStream_t stream);
 // Resident CTAs per SM for a variant at a given dynamic shared memory size.
 cudaError_t decode_occupancy(DecodeVariant v, int smem, int *ctas_per_sm);
 // Raise the dynamic shared memory limit of every variant (once per device).
 cudaError_t decode_configure_smem(int max_smem);
-// Dynamic shared memory bytes the combine kernel needs.
-size_t combine_smem_bytes(int num_splits, int D);
-// Raise the combine kernel's dynamic shared memory limit (once per device).
-cudaError_t combine_configure_smem(int max_smem);
 // Launch the combine kernel with programmatic dependent launch on `stream`.
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream);
 // Device error word of the current device.

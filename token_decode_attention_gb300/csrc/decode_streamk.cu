@@ -1,0 +1,591 @@
+// decode_streamk.cu -- fused stream-K decode attention for sm_103a.
+//
+// Computes, per sequence b and head h, the masked softmax attention of the
+// kernels attention_qk_f16 and attention_pv_f16 of "Developing Apple Metal
+// Kernels in Rust - A Deep Dive Through Attention" (section "The MSL, briefly")
+// in one pass over the live KV rows, without materialising scores:
+//   s_p  = (Q[b,h,:] . K[b,p,h,:]) / sqrt(D)         p < L_b = min(cp_b, S-1)+1
+//   out  = sum_p exp(s_p - max s) V[b,p,h,:] / sum_p exp(s_p - max s)
+//
+// Work split (stream-K, see streamk.h): the live positions of the whole batch,
+// flattened over (sequence, head group, position), are cut into G equal
+// ranges, one per CTA, and the grid is sized to the resident CTA slots of the
+// GPU.  Every CTA streams the same number of bytes whatever the mix of
+// sequence lengths, and there is no wave tail.  A range covers one or more
+// "pieces" (a run of positions of one unit); a CTA writes the f16 output of a
+// unit it covers whole and the partial softmax state (m, l, acc) of the others
+// for combine.cu.  Positions past L_b belong to no range: the page's -infinity
+// mask is a loop bound and masked rows are never read.
+//
+// Per CTA:
+//   * a producer warp streams, for each piece, stages of P positions: for the
+//     layout [B,S,H,D] the K rows of all heads of a run of positions are one
+//     contiguous span of HBM, moved by one bulk asynchronous copy
+//     (cp.async.bulk on the TMA engine, L2 evict-first) into a multi-stage
+//     shared-memory ring completing on mbarriers (V likewise);
+//   * eight consumer warps read each KV row with D/(8*CH) lanes, CH 16-byte
+//     shared loads per lane laid out so a lane group reads 128 contiguous
+//     bytes per load.  The QK product uses the raw f16 query and f16 keys with
+//     fp32 accumulation (products of two halves are exact in fp32); the dot is
+//     reduced with xor shuffles and scaled by log2(e)/sqrt(D).  Each lane group
+//     keeps an online softmax per (head, phase) slot in fp32 registers: the
+//     running max is only raised (and the state rescaled) when a new score
+//     exceeds it; PV accumulates with packed fp32x2 FMAs.
+//   * every mbarrier wait is bounded; a wait that runs out records an error in
+//     the device error word and the CTA returns after draining its copies.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "dattn_internal.h"
+#include "ptx.cuh"
+#include "streamk.h"
+
+namespace dattn {
+
+__device__ unsigned g_device_error = 0;
+
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per wait
+constexpr int kWarps = kDecodeThreads / 32;
+constexpr uint32_t kConsumerThreads = kConsumerWarps * 32;
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t polls = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        if ((++polls & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ int live_len(const uint32_t *cp, long long b, int S) {
+    const uint32_t c = __ldg(cp + b);
+    return c >= static_cast<uint32_t>(S - 1) ? S : static_cast<int>(c) + 1;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// d0 += q0*k0 + q2*k2 + q4*k4 + q6*k6 ; d1 += q1*k1 + q3*k3 + q5*k5 + q7*k7
+// with f16 inputs and fp32 accumulation (each product is exact in fp32).
+__device__ __forceinline__ void dot8(const uint4 q, const uint4 k, float &d0, float &d1) {
+    asm("{\n\t.reg .f16 qa, qb, ka, kb;\n\t"
+        "mov.b32 {qa, qb}, %2;\n\tmov.b32 {ka, kb}, %6;\n\t"
+        "fma.rn.f32.f16 %0, qa, ka, %0;\n\tfma.rn.f32.f16 %1, qb, kb, %1;\n\t"
+        "mov.b32 {qa, qb}, %3;\n\tmov.b32 {ka, kb}, %7;\n\t"
+        "fma.rn.f32.f16 %0, qa, ka, %0;\n\tfma.rn.f32.f16 %1, qb, kb, %1;\n\t"
+        "mov.b32 {qa, qb}, %4;\n\tmov.b32 {ka, kb}, %8;\n\t"
+        "fma.rn.f32.f16 %0, qa, ka, %0;\n\tfma.rn.f32.f16 %1, qb, kb, %1;\n\t"
+        "mov.b32 {qa, qb}, %5;\n\tmov.b32 {ka, kb}, %9;\n\t"
+        "fma.rn.f32.f16 %0, qa, ka, %0;\n\tfma.rn.f32.f16 %1, qb, kb, %1;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "r"(q.x), "r"(q.y), "r"(q.z), "r"(q.w), "r"(k.x), "r"(k.y), "r"(k.z), "r"(k.w));
+}
+
+// acc[0..7] += p * v[0..7]: v converted from f16, packed fp32x2 FMAs.
+__device__ __forceinline__ void axpy8(float *acc, float p, const uint4 v) {
+    asm("{\n\t.reg .f16 va, vb;\n\t.reg .f32 fa, fb;\n\t.reg .b64 x, c, pp;\n\t"
+        "mov.b64 pp, {%8, %8};\n\t"
+        "mov.b32 {va, vb}, %9;\n\tcvt.f32.f16 fa, va;\n\tcvt.f32.f16 fb, vb;\n\t"
+        "mov.b64 x, {fa, fb};\n\tmov.b64 c, {%0, %1};\n\tfma.rn.f32x2 c, x, pp, c;\n\t"
+        "mov.b64 {%0, %1}, c;\n\t"
+        "mov.b32 {va, vb}, %10;\n\tcvt.f32.f16 fa, va;\n\tcvt.f32.f16 fb, vb;\n\t"
+        "mov.b64 x, {fa, fb};\n\tmov.b64 c, {%2, %3};\n\tfma.rn.f32x2 c, x, pp, c;\n\t"
+        "mov.b64 {%2, %3}, c;\n\t"
+        "mov.b32 {va, vb}, %11;\n\tcvt.f32.f16 fa, va;\n\tcvt.f32.f16 fb, vb;\n\t"
+        "mov.b64 x, {fa, fb};\n\tmov.b64 c, {%4, %5};\n\tfma.rn.f32x2 c, x, pp, c;\n\t"
+        "mov.b64 {%4, %5}, c;\n\t"
+        "mov.b32 {va, vb}, %12;\n\tcvt.f32.f16 fa, va;\n\tcvt.f32.f16 fb, vb;\n\t"
+        "mov.b64 x, {fa, fb};\n\tmov.b64 c, {%6, %7};\n\tfma.rn.f32x2 c, x, pp, c;\n\t"
+        "mov.b64 {%6, %7}, c;\n\t}"
+        : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3]), "+f"(acc[4]), "+f"(acc[5]),
+          "+f"(acc[6]), "+f"(acc[7])
+        : "f"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+}
+
+__device__ __forceinline__ uint4 pack8_f16(const float *x, float s) {
+    uint4 r;
+    __half2 h;
+    h = __floats2half2_rn(x[0] * s, x[1] * s);
+    r.x = *reinterpret_cast<uint32_t *>(&h);
+    h = __floats2half2_rn(x[2] * s, x[3] * s);
+    r.y = *reinterpret_cast<uint32_t *>(&h);
+    h = __floats2half2_rn(x[4] * s, x[5] * s);
+    r.z = *reinterpret_cast<uint32_t *>(&h);
+    h = __floats2half2_rn(x[6] * s, x[7] * s);
+    r.w = *reinterpret_cast<uint32_t *>(&h);
+    return r;
+}
+
+// Walks the pieces of one CTA's range in flattened order (identically in the
+// producer and the consumers).
+struct Walker {
+    long long x, x1;   // next flattened position, end of the range
+    long long base;    // flattened position where sequence b starts
+    long long b;       // current sequence
+    int Lb;            // its live length
+    // current piece
+    int g, off, len;
+    long long u;
+};
+
+__device__ __forceinline__ bool next_piece(Walker &w, const DecodeArgs &a) {
+    if (w.x >= w.x1) return false;
+    const long long nhg = a.head_groups;
+    while (w.x >= w.base + nhg * w.Lb) {
+        w.base += nhg * w.Lb;
+        ++w.b;
+        w.Lb = live_len(a.cur_pos, w.b, a.S);
+    }
+    const long long rel = w.x - w.base;
+    w.g = static_cast<int>(rel / w.Lb);
+    w.off = static_cast<int>(rel - static_cast<long long>(w.g) * w.Lb);
+    const long long rest = w.x1 - w.x;
+    w.len = static_cast<int>(rest < w.Lb - w.off ? rest : w.Lb - w.off);
+    w.u = w.b * nhg + w.g;
+    w.x += w.len;
+    return true;
+}
+
+template <int BDX, int CH, int KMAX>
+__global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(CH, KMAX))
+    decode_streamk_kernel(const DecodeArgs a) {
+    constexpr int BDY = 32 / BDX;              // lane groups per warp
+    constexpr int NLG = kConsumerWarps * BDY;  // lane groups per CTA
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ long long s_warp_sum[kWarps];
+    __shared__ long long s_b0, s_base0;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int D = a.D;
+
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + a.bar_offset);
+    uint64_t *empty_bar = full_bar + a.stages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty_bar + a.stages);
+
+    // ---- the CTA's range: block scan of the live lengths over the batch ----
+    const long long per = (a.B + kDecodeThreads - 1) / kDecodeThreads;
+    const long long bb = min(static_cast<long long>(threadIdx.x) * per, static_cast<long long>(a.B));
+    const long long be = min(bb + per, static_cast<long long>(a.B));
+    long long sum = 0;
+    for (long long b = bb; b < be; ++b) sum += live_len(a.cur_pos, b, a.S);
+    long long incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp_sum[warp] = incl;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.stages; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], kConsumerWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    long long before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const long long v = s_warp_sum[w];
+        if (w < warp) before += v;
+        total += v;
+    }
+    const long long excl = before + incl - sum;
+    const long long nhg = a.head_groups;
+    const long long W = total * nhg;
+    const long long x0 = range_begin(blockIdx.x, W, a.partitions);
+    const long long x1 = range_begin(static_cast<long long>(blockIdx.x) + 1, W, a.partitions);
+    if (x0 < x1 && nhg * excl <= x0 && x0 < nhg * (excl + sum)) {
+        long long run = excl;
+        for (long long b = bb; b < be; ++b) {
+            const int L = live_len(a.cur_pos, b, a.S);
+            if (x0 < nhg * (run + L)) {
+                s_b0 = b;
+                s_base0 = nhg * run;
+                break;
+            }
+            run += L;
+        }
+    }
+    if (blockIdx.x == 0 && a.ws_prefix != nullptr) {
+        long long run = excl;
+        for (long long b = bb; b < be; ++b) {
+            a.ws_prefix[b] = run;
+            run += live_len(a.cur_pos, b, a.S);
+        }
+        if (threadIdx.x == 0) a.ws_prefix[a.B] = total;
+    }
+    __syncthreads();
+    // The combine kernel may begin launching; it waits for this grid to finish.
+    pdl_launch_dependents();
+    if (x0 >= x1) return;  // empty range (fewer live positions than CTAs)
+
+    Walker walk;
+    walk.x = x0;
+    walk.x1 = x1;
+    walk.b = s_b0;
+    walk.base = s_base0;
+    walk.Lb = live_len(a.cur_pos, walk.b, a.S);
+
+    __half *ring = reinterpret_cast<__half *>(smem);
+    const size_t buf_elems = static_cast<size_t>(a.stage_pos) * a.heads_per_cta * D;
+
+    if (warp == kConsumerWarps) {
+        // ---------------- producer warp ----------------
+        const uint64_t policy = l2_evict_first_policy();
+        const size_t pos_stride = static_cast<size_t>(a.H) * D;  // halves between positions
+        int st = 0, issued = 0;
+        bool go = true;
+        while (go && next_piece(walk, a)) {
+            const int h0 = walk.g * a.heads_per_cta;
+            const int hg = min(a.heads_per_cta, a.H - h0);
+            const size_t seq_base = (static_cast<size_t>(walk.b) * a.S * a.H + h0) * D;
+            const __half *Kb = reinterpret_cast<const __half *>(a.K) + seq_base;
+            const __half *Vb = reinterpret_cast<const __half *>(a.V) + seq_base;
+            const uint32_t row_bytes = static_cast<uint32_t>(hg) * D * 2;
+            const bool contiguous = (hg == a.H);
+            for (int p = 0; p < walk.len; p += a.stage_pos, ++st) {
+                const int slot = st % a.stages;
+                int ok = 1;
+                if (lane == 0) {
+                    if (st >= a.stages &&
+                        !wait_bounded(&empty_bar[slot], ((st / a.stages) - 1) & 1)) {
+                        atomicOr(a.err, kErrProducerWait);
+                        *abort_flag = 1;
+                        ok = 0;
+                    }
+                    if (*abort_flag) ok = 0;
+                }
+                ok = __shfl_sync(kFull, ok, 0);
+                if (!ok) {
+                    go = false;
+                    break;
+                }
+                const int np = min(a.stage_pos, walk.len - p);
+                const size_t pos0 = static_cast<size_t>(walk.off + p);
+                __half *dK = ring + static_cast<size_t>(slot) * 2 * buf_elems;
+                __half *dV = dK + buf_elems;
+                const __half *sK = Kb + pos0 * pos_stride;
+                const __half *sV = Vb + pos0 * pos_stride;
+                if (lane == 0) mbar_arrive_expect_tx(&full_bar[slot], 2u * np * row_bytes);
+                __syncwarp();
+                if (contiguous) {
+                    if (lane == 0) {
+                        bulk_g2s(dK, sK, np * row_bytes, &full_bar[slot], policy);
+                        bulk_g2s(dV, sV, np * row_bytes, &full_bar[slot], policy);
+                    }
+                } else {
+                    for (int j = lane; j < np; j += 32) {
+                        bulk_g2s(dK + static_cast<size_t>(j) * hg * D, sK + j * pos_stride,
+                                 row_bytes, &full_bar[slot], policy);
+                        bulk_g2s(dV + static_cast<size_t>(j) * hg * D, sV + j * pos_stride,
+                                 row_bytes, &full_bar[slot], policy);
+                    }
+                }
+                ++issued;
+            }
+        }
+        // Drain: no copy may still be landing in shared memory when the CTA exits.
+        if (lane == 0) {
+            for (int s = max(0, issued - a.stages); s < issued; ++s) {
+                if (!wait_bounded(&full_bar[s % a.stages], (s / a.stages) & 1))
+                    atomicOr(a.err, kErrDrainWait);
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumer warps ----------------
+    const int lig = lane % BDX;              // lane within its group
+    const int lg = warp * BDY + lane / BDX;  // lane group id in the CTA
+    const int nchunk = D >> 3;               // 8-element chunks per row
+    bool con[CH];
+#pragma unroll
+    for (int i = 0; i < CH; ++i) con[i] = lig + BDX * i < nchunk;
+
+    int hl[KMAX], ph[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+        const int s = lg + k * NLG;  // slot = phase * heads_per_cta + head
+        ph[k] = s / a.heads_per_cta;
+        hl[k] = s - ph[k] * a.heads_per_cta;
+    }
+    const int iters = a.stage_pos / a.phases;
+    float *mbuf = reinterpret_cast<float *>(smem + a.merge_offset);
+    const int rec = D + 2;
+    int st = 0;
+    // ok turns false (for the whole warp) once a pipeline wait has run out.  The
+    // warp then skips waits, compute and writes, but keeps walking the pieces
+    // and joining the consumers' named barriers, so no other warp can be left
+    // waiting on it.
+    bool ok = true;
+
+    while (next_piece(walk, a)) {
+        const int h0 = walk.g * a.heads_per_cta;
+        const int hg = min(a.heads_per_cta, a.H - h0);
+        const bool final_piece = (walk.off == 0 && walk.len == walk.Lb);
+        const long long slot_id = piece_slot(blockIdx.x, walk.u);
+        const __half *Qb =
+            reinterpret_cast<const __half *>(a.Q) + (static_cast<size_t>(walk.b) * a.H + h0) * D;
+
+        bool sv[KMAX];
+        uint4 q[KMAX][CH];
+        float acc[KMAX][CH * 8], m[KMAX], l[KMAX];
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+            sv[k] = ph[k] < a.phases && hl[k] < hg;
+            m[k] = -INFINITY;
+            l[k] = 0.f;
+#pragma unroll
+            for (int i = 0; i < CH * 8; ++i) acc[k][i] = 0.f;
+#pragma unroll
+            for (int i = 0; i < CH; ++i) {
+                q[k][i] = make_uint4(0u, 0u, 0u, 0u);
+                if (sv[k] && con[i])
+                    q[k][i] = ldg_nc_v4(Qb + static_cast<size_t>(hl[k]) * D + (lig + BDX * i) * 8);
+            }
+        }
+
+        for (int p = 0; p < walk.len; p += a.stage_pos, ++st) {
+            const int slot = st % a.stages;
+            if (ok) {
+                const bool done = wait_bounded(&full_bar[slot], (st / a.stages) & 1);
+                if (!__all_sync(kFull, done)) {
+                    if (lane == 0) atomicOr(a.err, kErrConsumerWait);
+                    *abort_flag = 1;
+                    ok = false;
+                }
+            }
+            if (!ok) continue;
+            const int np = min(a.stage_pos, walk.len - p);
+            const __half *sK = ring + static_cast<size_t>(slot) * 2 * buf_elems;
+            const __half *sV = sK + buf_elems;
+            for (int t = 0; t < iters; t += 2) {
+                float s0[KMAX], s1[KMAX];
+                bool v0[KMAX], v1[KMAX];
+                int r0[KMAX], r1[KMAX];
+#pragma unroll
+                for (int k = 0; k < KMAX; ++k) {
+                    const int j0 = ph[k] + t * a.phases;
+                    const int j1 = j0 + a.phases;
+                    v0[k] = sv[k] && j0 < np;
+                    v1[k] = sv[k] && (t + 1 < iters) && j1 < np;
+                    r0[k] = (j0 * hg + hl[k]) * D;
+                    r1[k] = (j1 * hg + hl[k]) * D;
+                    float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
+#pragma unroll
+                    for (int i = 0; i < CH; ++i) {
+                        if (con[i]) {
+                            const int c8 = (lig + BDX * i) * 8;
+                            if (v0[k]) dot8(q[k][i], *reinterpret_cast<const uint4 *>(sK + r0[k] + c8), a0, b0);
+                            if (v1[k]) dot8(q[k][i], *reinterpret_cast<const uint4 *>(sK + r1[k] + c8), a1, b1);
+                        }
+                    }
+                    s0[k] = a0 + b0;
+                    s1[k] = a1 + b1;
+                }
+#pragma unroll
+                for (int o = BDX / 2; o > 0; o >>= 1) {
+#pragma unroll
+                    for (int k = 0; k < KMAX; ++k) {
+                        s0[k] += __shfl_xor_sync(kFull, s0[k], o);
+                        s1[k] += __shfl_xor_sync(kFull, s1[k], o);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < KMAX; ++k) {
+                    if (!v0[k]) continue;  // v1 implies v0
+                    const float sc0 = s0[k] * a.qscale;
+                    const float sc1 = v1[k] ? s1[k] * a.qscale : -INFINITY;
+                    const float mx = fmaxf(sc0, sc1);
+                    if (mx > m[k]) {  // new running max: rescale the state
+                        const float alpha = fast_exp2(m[k] - mx);
+                        l[k] *= alpha;
+#pragma unroll
+                        for (int i = 0; i < CH * 8; ++i) acc[k][i] *= alpha;
+                        m[k] = mx;
+                    }
+                    const float p0 = fast_exp2(sc0 - m[k]);
+                    const float p1 = v1[k] ? fast_exp2(sc1 - m[k]) : 0.f;
+                    l[k] += p0 + p1;
+#pragma unroll
+                    for (int i = 0; i < CH; ++i) {
+                        if (con[i]) {
+                            const int c8 = (lig + BDX * i) * 8;
+                            axpy8(&acc[k][i * 8], p0, *reinterpret_cast<const uint4 *>(sV + r0[k] + c8));
+                            if (v1[k])
+                                axpy8(&acc[k][i * 8], p1, *reinterpret_cast<const uint4 *>(sV + r1[k] + c8));
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[slot]);
+        }
+        const bool write = ok && !*abort_flag;
+
+        // ---------------- piece epilogue ----------------
+        const size_t bh0 = static_cast<size_t>(walk.b) * a.H + h0;
+        if (a.phases == 1) {
+            // each slot is the only holder of its head: write from registers
+#pragma unroll
+            for (int k = 0; k < KMAX; ++k) {
+                if (!sv[k] || !write) continue;
+                if (final_piece) {
+                    const float inv = 1.f / l[k];
+#pragma unroll
+                    for (int i = 0; i < CH; ++i) {
+                        if (con[i]) {
+                            const int c8 = (lig + BDX * i) * 8;
+                            *reinterpret_cast<uint4 *>(reinterpret_cast<__half *>(a.out) +
+                                                       (bh0 + hl[k]) * D + c8) =
+                                pack8_f16(&acc[k][i * 8], inv);
+                        }
+                    }
+                } else {
+                    const size_t row = static_cast<size_t>(slot_id) * a.heads_per_cta + hl[k];
+#pragma unroll
+                    for (int i = 0; i < CH; ++i) {
+                        if (con[i]) {
+                            float4 *dst = reinterpret_cast<float4 *>(a.ws_acc + row * D +
+                                                                     (lig + BDX * i) * 8);
+                            dst[0] = make_float4(acc[k][i * 8 + 0], acc[k][i * 8 + 1],
+                                                 acc[k][i * 8 + 2], acc[k][i * 8 + 3]);
+                            dst[1] = make_float4(acc[k][i * 8 + 4], acc[k][i * 8 + 5],
+                                                 acc[k][i * 8 + 6], acc[k][i * 8 + 7]);
+                        }
+                    }
+                    if (lig == 0) a.ws_ml[row] = make_float2(m[k], l[k]);
+                }
+            }
+        } else {
+            // several lane groups share a head: merge their states in shared memory
+#pragma unroll
+            for (int k = 0; k < KMAX; ++k) {
+                if (!sv[k] || !write) continue;
+                float *r = mbuf + static_cast<size_t>(lg + k * NLG) * rec;
+                if (lig == 0) {
+                    r[0] = m[k];
+                    r[1] = l[k];
+                }
+#pragma unroll
+                for (int i = 0; i < CH; ++i) {
+                    if (con[i]) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) r[2 + (lig + BDX * i) * 8 + e] = acc[k][i * 8 + e];
+                    }
+                }
+            }
+            named_barrier_sync(1, kConsumerThreads);
+            const bool all_write = !*abort_flag;  // same for every consumer after the barrier
+            for (int idx = threadIdx.x; all_write && idx < hg * D; idx += kConsumerThreads) {
+                const int h = idx / D;
+                const int d = idx - h * D;
+                float M = -INFINITY;
+                for (int f = 0; f < a.phases; ++f) {
+                    const float *r = mbuf + static_cast<size_t>(f * a.heads_per_cta + h) * rec;
+                    if (r[1] > 0.f) M = fmaxf(M, r[0]);
+                }
+                float lsum = 0.f, num = 0.f;
+                for (int f = 0; f < a.phases; ++f) {
+                    const float *r = mbuf + static_cast<size_t>(f * a.heads_per_cta + h) * rec;
+                    if (r[1] > 0.f) {
+                        const float w = fast_exp2(r[0] - M);
+                        lsum = fmaf(w, r[1], lsum);
+                        num = fmaf(w, r[2 + d], num);
+                    }
+                }
+                if (final_piece) {
+                    reinterpret_cast<__half *>(a.out)[(bh0 + h) * D + d] = __float2half_rn(num / lsum);
+                } else {
+                    const size_t row = static_cast<size_t>(slot_id) * a.heads_per_cta + h;
+                    a.ws_acc[row * D + d] = num;
+                    if (d == 0) a.ws_ml[row] = make_float2(M, lsum);
+                }
+            }
+            named_barrier_sync(1, kConsumerThreads);
+        }
+    }
+}
+
+template <int BDX, int CH>
+const void *pick_kmax(int kmax) {
+    switch (kmax) {
+        case 1: return reinterpret_cast<const void *>(decode_streamk_kernel<BDX, CH, 1>);
+        case 2: return reinterpret_cast<const void *>(decode_streamk_kernel<BDX, CH, 2>);
+        case 3:
+            if constexpr (CH == 1) return reinterpret_cast<const void *>(decode_streamk_kernel<BDX, CH, 3>);
+            return nullptr;
+        case 4:
+            if constexpr (CH == 1) return reinterpret_cast<const void *>(decode_streamk_kernel<BDX, CH, 4>);
+            return nullptr;
+        default: return nullptr;
+    }
+}
+
+const void *variant_fn(DecodeVariant v) {
+    if (v.ch == 1) {
+        switch (v.bdx) {
+            case 1: return pick_kmax<1, 1>(v.kmax);
+            case 2: return pick_kmax<2, 1>(v.kmax);
+            case 4: return pick_kmax<4, 1>(v.kmax);
+            case 8: return pick_kmax<8, 1>(v.kmax);
+            default: return nullptr;
+        }
+    }
+    if (v.ch == 2) {
+        switch (v.bdx) {
+            case 8: return pick_kmax<8, 2>(v.kmax);
+            case 16: return pick_kmax<16, 2>(v.kmax);
+            default: return nullptr;
+        }
+    }
+    return nullptr;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &a, DecodeVariant v, int smem, cudaStream_t stream) {
+    const void *fn = variant_fn(v);
+    if (fn == nullptr || a.partitions <= 0) return cudaErrorInvalidValue;
+    void *args[] = {const_cast<DecodeArgs *>(&a)};
+    return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(a.partitions)), dim3(kDecodeThreads),
+                            args, static_cast<size_t>(smem), stream);
+}
+
+cudaError_t decode_occupancy(DecodeVariant v, int smem, int *ctas_per_sm) {
+    const void *fn = variant_fn(v);
+    if (fn == nullptr) return cudaErrorInvalidValue;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, kDecodeThreads,
+                                                         static_cast<size_t>(smem));
+}
+
+cudaError_t decode_configure_smem(int max_smem) {
+    static const DecodeVariant variants[] = {
+        {1, 1, 1}, {1, 1, 2}, {1, 1, 3}, {1, 1, 4}, {2, 1, 1}, {2, 1, 2}, {2, 1, 3}, {2, 1, 4},
+        {4, 1, 1}, {4, 1, 2}, {4, 1, 3}, {4, 1, 4}, {8, 1, 1}, {8, 1, 2}, {8, 1, 3}, {8, 1, 4},
+        {8, 2, 1}, {8, 2, 2}, {16, 2, 1}, {16, 2, 2}};
+    for (const DecodeVariant &v : variants) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            variant_fn(v), cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t device_error_word(unsigned **ptr) {
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(ptr), g_device_error);
+}
+
+}  // namespace dattn
