@@ -36,6 +36,7 @@ constexpr int kStageTargetBytes = 32 * 1024;
 constexpr int kTwoPerSmBudget = 110 * 1024;  // ring bytes per CTA at 2 CTAs/SM
 constexpr int kOnePerSmBudget = 200 * 1024;  // ring bytes per CTA at 1 CTA/SM
 constexpr int kMaxStages = 12;
+constexpr int kStaticSmemReserve = 1024;  // the decode kernel's static shared memory
 
 thread_local std::string g_last_error;
 
@@ -199,7 +200,7 @@ int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
     p.merge_offset = p.NST * stage_bytes;
     p.bar_offset = round_up(p.merge_offset + merge_bytes, 16);
     p.smem = p.bar_offset + p.NST * 16 + 16;
-    if (p.smem > di.max_smem_optin)
+    if (p.smem > di.max_smem_optin - kStaticSmemReserve)
         return fail(DATTN_ERR_UNSUPPORTED, "shape needs %d B of shared memory (limit %d)",
                     p.smem, di.max_smem_optin);
     cudaError_t e = dattn::decode_occupancy(p.v, p.smem, &p.ctas_per_sm);

@@ -577,8 +577,12 @@ cudaError_t decode_configure_smem(int max_smem) {
         {4, 1, 1}, {4, 1, 2}, {4, 1, 3}, {4, 1, 4}, {8, 1, 1}, {8, 1, 2}, {8, 1, 3}, {8, 1, 4},
         {8, 2, 1}, {8, 2, 2}, {16, 2, 1}, {16, 2, 2}};
     for (const DecodeVariant &v : variants) {
-        const cudaError_t e = cudaFuncSetAttribute(
-            variant_fn(v), cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        // static and dynamic shared memory together may not exceed the opt-in limit
+        cudaFuncAttributes attr{};
+        cudaError_t e = cudaFuncGetAttributes(&attr, variant_fn(v));
+        if (e != cudaSuccess) return e;
+        const int dyn = max_smem - static_cast<int>(attr.sharedSizeBytes);
+        e = cudaFuncSetAttribute(variant_fn(v), cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
