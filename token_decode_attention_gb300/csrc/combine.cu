@@ -10,9 +10,13 @@
 // Units held by a single partition already have their output written by the
 // decode kernel and are skipped.
 //
-// Grid: one CTA per (sequence, head, chunk of 32 channels), so even a single
-// long sequence spreads its merge over H * D/32 CTAs; inside a CTA, threads
-// take (piece, float4) pairs and keep several loads in flight.  Launched with
+// Grid: one CTA per (sequence, head, chunk of channels).  The host picks the
+// chunk width from the expected number of pieces per unit: whole heads when
+// units have few pieces (many sequences), narrow chunks when one sequence is
+// spread over every partition, so each thread folds only a few pieces.  Each
+// thread folds its pieces online (running max, rescaled sum and accumulator)
+// after issuing their loads together; the per-thread states are folded once
+// more through shared memory.  Launched with
 // programmatic dependent launch: it may start while the decode kernel drains
 // and waits on griddepcontrol.wait before touching the workspace.
 #include <cuda_fp16.h>
@@ -27,9 +31,7 @@
 namespace dattn {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 32;  // channels per CTA
+constexpr int kThreads = 128;
 
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -37,11 +39,32 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) {
-    __shared__ float red[kWarps];
-    __shared__ float4 part[kThreads];
+// Fold one state (m, l, acc) into a running state, rescaling whichever of the
+// two has the smaller maximum.
+__device__ __forceinline__ void fold(float &M, float &L, float4 &A, float m, float l, float4 a) {
+    if (l <= 0.f) return;
+    if (m > M) {
+        const float s = fast_exp2(M - m);  // 0 when M is -inf
+        L *= s;
+        A.x *= s;
+        A.y *= s;
+        A.z *= s;
+        A.w *= s;
+        M = m;
+    }
+    const float w = fast_exp2(m - M);
+    L = fmaf(w, l, L);
+    A.x = fmaf(w, a.x, A.x);
+    A.y = fmaf(w, a.y, A.y);
+    A.z = fmaf(w, a.z, A.z);
+    A.w = fmaf(w, a.w, A.w);
+}
 
-    const int nchunks = (a.D + kChunk - 1) / kChunk;
+__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) {
+    __shared__ float sm_m[kThreads], sm_l[kThreads];
+    __shared__ float4 sm_a[kThreads];
+
+    const int nchunks = (a.D + a.chunk - 1) / a.chunk;
     const long long idx = blockIdx.x;
     const int chunk = static_cast<int>(idx % nchunks);
     const long long bh = idx / nchunks;
@@ -63,87 +86,51 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
     if (c_first == c_last) return;  // written whole by the decode kernel
     const int npieces = static_cast<int>(c_last - c_first + 1);
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const size_t hg_stride = a.heads_per_cta;
-    auto ml_of = [&](int j) -> float2 {
-        return a.ws_ml[static_cast<size_t>(piece_slot(c_first + j, u)) * hg_stride + hl];
-    };
-
-    float M = -INFINITY;
-    for (int j = tid; j < npieces; j += kThreads) M = fmaxf(M, ml_of(j).x);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if (lane == 0) red[warp] = M;
-    __syncthreads();
-    M = red[0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, red[w]);
-    __syncthreads();
-
-    float lsum = 0.f;
-    for (int j = tid; j < npieces; j += kThreads) {
-        const float2 v = ml_of(j);
-        lsum = fmaf(fast_exp2(v.x - M), v.y, lsum);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-    if (lane == 0) red[warp] = lsum;
-    __syncthreads();
-    lsum = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) lsum += red[w];
-
-    // weighted sum of the partial accumulators for this chunk of channels
-    const int c0 = chunk * kChunk;
-    const int width = min(kChunk, a.D - c0);  // a multiple of 8
-    const int f4 = width / 4;                 // float4 per piece row
-    const int nsub = kThreads / f4;           // pieces in flight per pass
+    const int tid = threadIdx.x;
+    const int c0 = chunk * a.chunk;
+    const int width = min(a.chunk, a.D - c0);  // a multiple of 8
+    const int f4 = width / 4;                  // float4 per piece row
+    const int nsub = kThreads / f4;            // pieces in flight
     const int sub = tid / f4, f = tid - sub * f4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const size_t hgs = a.heads_per_cta;
+
+    float M = -INFINITY, L = 0.f;
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
     if (sub < nsub) {
         int j = sub;
         for (; j + 3 * nsub < npieces; j += 4 * nsub) {
+            float2 ml[4];
             float4 v[4];
-            float w[4];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
-                const int jj = j + r * nsub;
-                const size_t row = static_cast<size_t>(piece_slot(c_first + jj, u)) * hg_stride + hl;
+                const size_t row = static_cast<size_t>(piece_slot(c_first + j + r * nsub, u)) * hgs + hl;
+                ml[r] = a.ws_ml[row];
                 v[r] = *reinterpret_cast<const float4 *>(a.ws_acc + row * a.D + c0 + f * 4);
-                w[r] = fast_exp2(a.ws_ml[row].x - M);
             }
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                acc.x = fmaf(w[r], v[r].x, acc.x);
-                acc.y = fmaf(w[r], v[r].y, acc.y);
-                acc.z = fmaf(w[r], v[r].z, acc.z);
-                acc.w = fmaf(w[r], v[r].w, acc.w);
-            }
+            for (int r = 0; r < 4; ++r) fold(M, L, A, ml[r].x, ml[r].y, v[r]);
         }
         for (; j < npieces; j += nsub) {
-            const size_t row = static_cast<size_t>(piece_slot(c_first + j, u)) * hg_stride + hl;
+            const size_t row = static_cast<size_t>(piece_slot(c_first + j, u)) * hgs + hl;
+            const float2 ml = a.ws_ml[row];
             const float4 v = *reinterpret_cast<const float4 *>(a.ws_acc + row * a.D + c0 + f * 4);
-            const float w = fast_exp2(a.ws_ml[row].x - M);
-            acc.x = fmaf(w, v.x, acc.x);
-            acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z);
-            acc.w = fmaf(w, v.w, acc.w);
+            fold(M, L, A, ml.x, ml.y, v);
         }
     }
-    part[tid] = acc;
+    sm_m[tid] = M;
+    sm_l[tid] = L;
+    sm_a[tid] = A;
     __syncthreads();
     if (tid < f4) {
-        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        float M2 = -INFINITY, L2 = 0.f;
+        float4 A2 = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int r = 0; r < nsub; ++r) {
-            const float4 v = part[r * f4 + tid];
-            s.x += v.x;
-            s.y += v.y;
-            s.z += v.z;
-            s.w += v.w;
+            const int t = r * f4 + tid;
+            fold(M2, L2, A2, sm_m[t], sm_l[t], sm_a[t]);
         }
-        const float inv = 1.f / lsum;
-        __half2 lo = __floats2half2_rn(s.x * inv, s.y * inv);
-        __half2 hi = __floats2half2_rn(s.z * inv, s.w * inv);
+        const float inv = 1.f / L2;
+        __half2 lo = __floats2half2_rn(A2.x * inv, A2.y * inv);
+        __half2 hi = __floats2half2_rn(A2.z * inv, A2.w * inv);
         uint2 packed;
         packed.x = *reinterpret_cast<uint32_t *>(&lo);
         packed.y = *reinterpret_cast<uint32_t *>(&hi);
@@ -155,7 +142,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream) {
-    const long long blocks = static_cast<long long>(a.B) * a.H * ((a.D + kChunk - 1) / kChunk);
+    if (a.chunk <= 0 || a.chunk % 8 != 0) return cudaErrorInvalidValue;
+    const long long blocks = static_cast<long long>(a.B) * a.H * ((a.D + a.chunk - 1) / a.chunk);
     if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));

@@ -103,6 +103,7 @@ struct Plan {
     int HG = 0, NHG = 0, PHI = 0, P = 0, NST = 0, G = 0;
     int smem = 0, merge_offset = 0, bar_offset = 0, ctas_per_sm = 0, sms = 0;
     size_t prefix_bytes = 0, acc_bytes = 0, ws_bytes = 0;
+    int combine_chunk = 0;  // channels per combine CTA
 };
 
 int next_pow2(int x) {
@@ -177,21 +178,26 @@ int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
         bdx = 16;
         ch = 2;
     }
-    const int nlg = dattn::kConsumerWarps * (32 / bdx);  // lane groups per CTA
-    const int kmax_cap = ch == 2 ? 2 : 4;
-    const int hg_max = std::min(nlg * kmax_cap, std::max(1, kMaxRowBytesKV / (D * 4)));
+    // Eight consumer warps (two CTAs per SM) while the heads fit their register
+    // slots; otherwise sixteen (one CTA per SM, same warps per SM); beyond that
+    // the heads are split into groups handled by different CTAs.
+    const int kcap = ch == 2 ? 1 : 2;  // register slots per lane group
+    int nwc = 8;
+    if (H > nwc * (32 / bdx) * kcap) nwc = 16;
+    const int nlg = nwc * (32 / bdx);  // lane groups per CTA
+    const int hg_max = std::min(nlg * kcap, std::max(1, kMaxRowBytesKV / (D * 4)));
     p.NHG = (H + hg_max - 1) / hg_max;
     p.HG = (H + p.NHG - 1) / p.NHG;
     p.PHI = p.HG >= nlg ? 1 : std::min(32, nlg / p.HG);
     const int kmax = (p.HG * p.PHI + nlg - 1) / nlg;
-    p.v = DecodeVariant{bdx, ch, kmax};
+    p.v = DecodeVariant{bdx, ch, kmax, nwc};
     const int row_bytes = p.HG * D * 2;
     int P = std::max(1, std::min(256, kStageTargetBytes / 2 / row_bytes));
     P = std::max(p.PHI, P / p.PHI * p.PHI);
     p.P = P;
     const int stage_bytes = 2 * P * row_bytes;
     const int merge_bytes = p.PHI > 1 ? p.HG * p.PHI * (D + 2) * 4 : 0;
-    const int ring_budget = dattn::decode_min_blocks(ch, kmax) == 2
+    const int ring_budget = dattn::decode_min_blocks(nwc) == 2
                                 ? kTwoPerSmBudget - merge_bytes
                                 : kOnePerSmBudget - merge_bytes;
     int nst = ring_budget / stage_bytes;
@@ -220,6 +226,12 @@ int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
         p.prefix_bytes = round_up_sz((static_cast<size_t>(B) + 1) * sizeof(long long), 256);
         p.acc_bytes = round_up_sz(rows * D * sizeof(float), 256);
         p.ws_bytes = p.prefix_bytes + p.acc_bytes + rows * sizeof(float2);
+        // Combine chunk: at most ~8 pieces per thread of a 128-thread CTA, given
+        // the expected pieces per unit (G + U) / U.
+        const double pieces = static_cast<double>(p.G + units) / static_cast<double>(units);
+        int cw = std::min(256, next_pow2(D));
+        while (cw > 8 && pieces * cw / 512.0 > 8.0) cw /= 2;
+        p.combine_chunk = cw;
     }
     {
         std::lock_guard<std::mutex> lock(g_plan_mutex);
@@ -288,6 +300,7 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
         c.heads_per_cta = p.HG;
         c.head_groups = p.NHG;
         c.partitions = p.G;
+        c.chunk = p.combine_chunk;
         e = dattn::launch_combine(c, stream);
         if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return fail_cuda(e, "combine kernel launch");
@@ -338,7 +351,7 @@ int dattn_decode_plan(int batch, int n_heads, int head_dim, int seq_len, int num
     plan->head_groups = p.NHG;
     plan->stage_positions = p.P;
     plan->stages = p.NST;
-    plan->threads_per_cta = dattn::kDecodeThreads;
+    plan->threads_per_cta = dattn::decode_threads(p.v.nwc);
     plan->smem_bytes = p.smem;
     plan->ctas_per_sm = p.ctas_per_sm;
     plan->sm_count = p.sms;

@@ -9,10 +9,10 @@
 
 namespace dattn {
 
-// Consumer warps per CTA of the decode kernel; one more warp issues the bulk
-// copies.
-constexpr int kConsumerWarps = 8;
-constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+// Threads of a decode CTA with `nwc` consumer warps: one more warp issues the
+// bulk copies.  Eight consumer warps run two CTAs per SM, sixteen run one.
+__host__ __device__ constexpr int decode_threads(int nwc) { return (nwc + 1) * 32; }
+__host__ __device__ constexpr int decode_min_blocks(int nwc) { return nwc <= 8 ? 2 : 1; }
 
 // Error codes a kernel records in the device error word.
 constexpr unsigned kErrConsumerWait = 1u;
@@ -60,20 +60,16 @@ struct CombineArgs {
     int heads_per_cta;
     int head_groups;
     int partitions;
+    int chunk;  // channels per combine CTA (a multiple of 8)
 };
 
 // Compile-time shape of one decode-kernel instance.
 struct DecodeVariant {
     int bdx;   // lanes per KV row: 1, 2, 4, 8 (chunks = 1) or 8, 16 (chunks = 2)
     int ch;    // 8-element chunks per lane: 1 or 2
-    int kmax;  // (head, phase) slots per lane group: 1..4 (1..2 when ch = 2)
+    int kmax;  // (head, phase) slots per lane group: 1..2 (1 when ch = 2)
+    int nwc;   // consumer warps: 8 or 16
 };
-
-// CTAs per SM a variant is compiled for.  Variants that keep three or more
-// 8-channel state blocks per lane are compiled for one CTA per SM, so they get
-// enough registers not to spill, and use a deeper shared-memory ring instead
-// of a second CTA.
-constexpr int decode_min_blocks(int ch, int kmax) { return ch * kmax >= 3 ? 1 : 2; }
 
 // Launch the decode kernel.  smem = dynamic shared memory bytes.
 cudaError_t launch_decode(const DecodeArgs &a, DecodeVariant v, int smem, cudaStream_t stream);

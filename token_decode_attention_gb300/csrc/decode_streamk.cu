@@ -49,8 +49,6 @@ __device__ unsigned g_device_error = 0;
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per wait
-constexpr int kWarps = kDecodeThreads / 32;
-constexpr uint32_t kConsumerThreads = kConsumerWarps * 32;
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity) {
@@ -155,11 +153,14 @@ __device__ __forceinline__ bool next_piece(Walker &w, const DecodeArgs &a) {
     return true;
 }
 
-template <int BDX, int CH, int KMAX>
-__global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(CH, KMAX))
+template <int BDX, int CH, int KMAX, int NWC>
+__global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     decode_streamk_kernel(const DecodeArgs a) {
-    constexpr int BDY = 32 / BDX;              // lane groups per warp
-    constexpr int NLG = kConsumerWarps * BDY;  // lane groups per CTA
+    constexpr int BDY = 32 / BDX;        // lane groups per warp
+    constexpr int NLG = NWC * BDY;       // lane groups per CTA
+    constexpr int kThreads = decode_threads(NWC);
+    constexpr int kWarps = NWC + 1;
+    constexpr uint32_t kConsumerThreads = NWC * 32;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ long long s_warp_sum[kWarps];
     __shared__ long long s_b0, s_base0;
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(CH, KMAX))
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty_bar + a.stages);
 
     // ---- the CTA's range: block scan of the live lengths over the batch ----
-    const long long per = (a.B + kDecodeThreads - 1) / kDecodeThreads;
+    const long long per = (a.B + kThreads - 1) / kThreads;
     const long long bb = min(static_cast<long long>(threadIdx.x) * per, static_cast<long long>(a.B));
     const long long be = min(bb + per, static_cast<long long>(a.B));
     long long sum = 0;
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(CH, KMAX))
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.stages; ++i) {
             mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], kConsumerWarps);
+            mbar_init(&empty_bar[i], NWC);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(CH, KMAX))
     __half *ring = reinterpret_cast<__half *>(smem);
     const size_t buf_elems = static_cast<size_t>(a.stage_pos) * a.heads_per_cta * D;
 
-    if (warp == kConsumerWarps) {
+    if (warp == NWC) {
         // ---------------- producer warp ----------------
         const uint64_t policy = l2_evict_first_policy();
         const size_t pos_stride = static_cast<size_t>(a.H) * D;  // halves between positions
@@ -519,38 +520,45 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(CH, KMAX))
     }
 }
 
-template <int BDX, int CH>
+// Instances: lanes per row x chunks per lane x slots per lane group x consumer
+// warps.  Eight consumer warps (two CTAs per SM) up to one slot of two chunks
+// or two slots of one chunk per lane group; sixteen consumer warps (one CTA per
+// SM, the same warps per SM) when a CTA must hold more heads.
+template <int BDX, int CH, int NWC>
 const void *pick_kmax(int kmax) {
     switch (kmax) {
-        case 1: return reinterpret_cast<const void *>(decode_streamk_kernel<BDX, CH, 1>);
-        case 2: return reinterpret_cast<const void *>(decode_streamk_kernel<BDX, CH, 2>);
-        case 3:
-            if constexpr (CH == 1) return reinterpret_cast<const void *>(decode_streamk_kernel<BDX, CH, 3>);
-            return nullptr;
-        case 4:
-            if constexpr (CH == 1) return reinterpret_cast<const void *>(decode_streamk_kernel<BDX, CH, 4>);
+        case 1: return reinterpret_cast<const void *>(decode_streamk_kernel<BDX, CH, 1, NWC>);
+        case 2:
+            if constexpr (CH == 1) return reinterpret_cast<const void *>(decode_streamk_kernel<BDX, CH, 2, NWC>);
             return nullptr;
         default: return nullptr;
     }
 }
 
+template <int NWC>
+const void *pick_shape(int bdx, int ch, int kmax) {
+    if (ch == 1) {
+        switch (bdx) {
+            case 1: return pick_kmax<1, 1, NWC>(kmax);
+            case 2: return pick_kmax<2, 1, NWC>(kmax);
+            case 4: return pick_kmax<4, 1, NWC>(kmax);
+            case 8: return pick_kmax<8, 1, NWC>(kmax);
+            default: return nullptr;
+        }
+    }
+    if (ch == 2) {
+        switch (bdx) {
+            case 8: return pick_kmax<8, 2, NWC>(kmax);
+            case 16: return pick_kmax<16, 2, NWC>(kmax);
+            default: return nullptr;
+        }
+    }
+    return nullptr;
+}
+
 const void *variant_fn(DecodeVariant v) {
-    if (v.ch == 1) {
-        switch (v.bdx) {
-            case 1: return pick_kmax<1, 1>(v.kmax);
-            case 2: return pick_kmax<2, 1>(v.kmax);
-            case 4: return pick_kmax<4, 1>(v.kmax);
-            case 8: return pick_kmax<8, 1>(v.kmax);
-            default: return nullptr;
-        }
-    }
-    if (v.ch == 2) {
-        switch (v.bdx) {
-            case 8: return pick_kmax<8, 2>(v.kmax);
-            case 16: return pick_kmax<16, 2>(v.kmax);
-            default: return nullptr;
-        }
-    }
+    if (v.nwc == 8) return pick_shape<8>(v.bdx, v.ch, v.kmax);
+    if (v.nwc == 16) return pick_shape<16>(v.bdx, v.ch, v.kmax);
     return nullptr;
 }
 
@@ -560,22 +568,23 @@ cudaError_t launch_decode(const DecodeArgs &a, DecodeVariant v, int smem, cudaSt
     const void *fn = variant_fn(v);
     if (fn == nullptr || a.partitions <= 0) return cudaErrorInvalidValue;
     void *args[] = {const_cast<DecodeArgs *>(&a)};
-    return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(a.partitions)), dim3(kDecodeThreads),
-                            args, static_cast<size_t>(smem), stream);
+    return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(a.partitions)),
+                            dim3(decode_threads(v.nwc)), args, static_cast<size_t>(smem), stream);
 }
 
 cudaError_t decode_occupancy(DecodeVariant v, int smem, int *ctas_per_sm) {
     const void *fn = variant_fn(v);
     if (fn == nullptr) return cudaErrorInvalidValue;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, kDecodeThreads,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, decode_threads(v.nwc),
                                                          static_cast<size_t>(smem));
 }
 
 cudaError_t decode_configure_smem(int max_smem) {
     static const DecodeVariant variants[] = {
-        {1, 1, 1}, {1, 1, 2}, {1, 1, 3}, {1, 1, 4}, {2, 1, 1}, {2, 1, 2}, {2, 1, 3}, {2, 1, 4},
-        {4, 1, 1}, {4, 1, 2}, {4, 1, 3}, {4, 1, 4}, {8, 1, 1}, {8, 1, 2}, {8, 1, 3}, {8, 1, 4},
-        {8, 2, 1}, {8, 2, 2}, {16, 2, 1}, {16, 2, 2}};
+        {1, 1, 1, 8},  {1, 1, 2, 8},  {2, 1, 1, 8},  {2, 1, 2, 8},  {4, 1, 1, 8},
+        {4, 1, 2, 8},  {8, 1, 1, 8},  {8, 1, 2, 8},  {8, 2, 1, 8},  {16, 2, 1, 8},
+        {1, 1, 1, 16}, {1, 1, 2, 16}, {2, 1, 1, 16}, {2, 1, 2, 16}, {4, 1, 1, 16},
+        {4, 1, 2, 16}, {8, 1, 1, 16}, {8, 1, 2, 16}, {8, 2, 1, 16}, {16, 2, 1, 16}};
     for (const DecodeVariant &v : variants) {
         // static and dynamic shared memory together may not exceed the opt-in limit
         cudaFuncAttributes attr{};
