@@ -158,14 +158,21 @@ def barrier(world: int):
 class Replica:
     """Input sets, outputs and workspace of one workload on one GPU."""
 
-    def __init__(self, name: str, device, l2_bytes: int, partitions: int = 0):
+    def __init__(self, name: str, device, l2_bytes: int, partitions: int = 0,
+                 batch: int = 0):
+        import dataclasses
+
         import token_decode_attention_gb300 as dattn
         self.dattn = dattn
         self.w = w = WORKLOADS[name]
+        if batch:
+            # same per-sequence recipe, fewer sequences (small ncu captures)
+            self.w = w = dataclasses.replace(w, batch=batch,
+                                             description=w.description + f", batch {batch}")
         self.device = device
         kv = w.kv_bytes()
         self.sets_n = 1 if kv >= 4 * l2_bytes else min(4096, math.ceil(4 * l2_bytes / kv) + 1)
-        base = make_inputs(w, device)
+        base = make_inputs(WORKLOADS[name], device, batch=w.batch)
         self.cp_host = base["cur_pos_host"]
         self.sets = [base]
         for i in range(1, self.sets_n):
@@ -388,6 +395,8 @@ def main():
                     help="issue the timed steps from Python instead of a CUDA graph")
     ap.add_argument("--partitions", type=int, default=0,
                     help="force the number of decode partitions (0 = library choice)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="with --profile: fewer sequences of the same recipe")
     ap.add_argument("--profile", action="store_true",
                     help="only warm-up and timed steps of one workload (for ncu captures)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -417,7 +426,8 @@ def main():
     peak, peak_kind = hbm_peak()
     stream = torch.cuda.Stream(device=device)
 
-    rep = Replica(args.workload, device, l2, args.partitions)
+    rep = Replica(args.workload, device, l2, args.partitions,
+                  args.batch if args.profile else 0)
     sampler = ClockSampler(local)
     if args.profile:
         ms, _ = rep.timed(args.steps, args.warmup, stream, world, soak_s=0.0,
