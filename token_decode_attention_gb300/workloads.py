@@ -118,7 +118,7 @@ def make_inputs(w: Workload, device: str | torch.device = "cuda", seed: int | No
         kv = k.view(B * w.seq_len, w.n_heads, w.head_dim)
         kv[:, heads.reshape(-1), ch.reshape(-1)] *= w.outlier_scale
     cp = draw_current_pos(w, seed)
-    if batch is not None and w.current_pos is None:
+    if batch is not None:
         cp = np.resize(cp, B).astype(np.uint32)
     cp_dev = torch.from_numpy(cp.astype(np.int64)).to(torch.int32).to(device)
     return {"q": q, "k": k, "v": v, "cur_pos": cp_dev, "cur_pos_host": cp}
