@@ -32,7 +32,8 @@ constexpr long long kMinPositions = 16;  // positions per partition chosen by th
 constexpr int kMaxHeadDim = 256;
 constexpr int kMaxHeadsPerLaneGroup = 4;  // register slots per lane group (KMAX)
 constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
-constexpr int kStageTargetBytes = 32 * 1024;
+constexpr int kStageTargetBytes = 32 * 1024;          // K+V per stage, 2 CTAs/SM
+constexpr int kStageTargetBytesOnePerSm = 40 * 1024;  // K+V per stage, 1 CTA/SM
 constexpr int kTwoPerSmBudget = 110 * 1024;  // ring bytes per CTA at 2 CTAs/SM
 constexpr int kOnePerSmBudget = 200 * 1024;  // ring bytes per CTA at 1 CTA/SM
 constexpr int kMaxStages = 12;
@@ -100,7 +101,7 @@ int device_info(DeviceInfo *out) {
 
 struct Plan {
     DecodeVariant v{};
-    int HG = 0, NHG = 0, PHI = 0, P = 0, NST = 0, G = 0;
+    int HG = 0, NHG = 0, PHI = 0, P = 0, NST = 0, G = 0, active_warps = 0;
     int smem = 0, merge_offset = 0, bar_offset = 0, ctas_per_sm = 0, sms = 0;
     size_t prefix_bytes = 0, acc_bytes = 0, ws_bytes = 0;
     int combine_chunk = 0;  // channels per combine CTA
@@ -191,8 +192,11 @@ int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
     p.PHI = p.HG >= nlg ? 1 : std::min(32, nlg / p.HG);
     const int kmax = (p.HG * p.PHI + nlg - 1) / nlg;
     p.v = DecodeVariant{bdx, ch, kmax, nwc};
+    // warps whose first lane group holds a slot (slot s = lane group + k * nlg)
+    p.active_warps = std::min(nwc, (p.HG * p.PHI + (32 / bdx) - 1) / (32 / bdx));
     const int row_bytes = p.HG * D * 2;
-    int P = std::max(1, std::min(256, kStageTargetBytes / 2 / row_bytes));
+    const int stage_target = nwc == 8 ? kStageTargetBytes : kStageTargetBytesOnePerSm;
+    int P = std::max(1, std::min(256, stage_target / 2 / row_bytes));
     P = std::max(p.PHI, P / p.PHI * p.PHI);
     p.P = P;
     const int stage_bytes = 2 * P * row_bytes;
@@ -280,6 +284,7 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
     a.stage_pos = p.P;
     a.stages = p.NST;
     a.partitions = p.G;
+    a.active_warps = p.active_warps;
     a.merge_offset = p.merge_offset;
     a.bar_offset = p.bar_offset;
     a.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));

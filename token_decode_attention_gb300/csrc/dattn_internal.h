@@ -44,6 +44,7 @@ struct DecodeArgs {
     int stage_pos;      // P: positions per pipeline stage (a multiple of PHI)
     int stages;         // NST: pipeline depth
     int partitions;     // G: CTAs
+    int active_warps;   // consumer warps holding at least one (head, phase) slot
     int merge_offset;   // byte offset of the phase-merge area in dynamic smem
     int bar_offset;     // byte offset of the mbarriers in dynamic smem
     float qscale;       // log2(e) / sqrt(D), applied to each dot product

@@ -54,9 +54,8 @@ constexpr unsigned kFull = 0xffffffffu;
 __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    uint32_t polls = 0;
     while (!mbar_try_wait(bar, parity)) {
-        if ((++polls & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
     return true;
 }
@@ -160,10 +159,10 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     constexpr int NLG = NWC * BDY;       // lane groups per CTA
     constexpr int kThreads = decode_threads(NWC);
     constexpr int kWarps = NWC + 1;
-    constexpr uint32_t kConsumerThreads = NWC * 32;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ long long s_warp_sum[kWarps];
     __shared__ long long s_b0, s_base0;
+    __shared__ int s_L0;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -189,7 +188,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.stages; ++i) {
             mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], NWC);
+            mbar_init(&empty_bar[i], a.active_warps);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -214,6 +213,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
             if (x0 < nhg * (run + L)) {
                 s_b0 = b;
                 s_base0 = nhg * run;
+                s_L0 = L;
                 break;
             }
             run += L;
@@ -231,13 +231,15 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     // The combine kernel may begin launching; it waits for this grid to finish.
     pdl_launch_dependents();
     if (x0 >= x1) return;  // empty range (fewer live positions than CTAs)
+    // consumer warps whose lane groups hold no (head, phase) slot have nothing to do
+    if (warp < NWC && warp >= a.active_warps) return;
 
     Walker walk;
     walk.x = x0;
     walk.x1 = x1;
     walk.b = s_b0;
     walk.base = s_base0;
-    walk.Lb = live_len(a.cur_pos, walk.b, a.S);
+    walk.Lb = s_L0;
 
     __half *ring = reinterpret_cast<__half *>(smem);
     const size_t buf_elems = static_cast<size_t>(a.stage_pos) * a.heads_per_cta * D;
@@ -323,6 +325,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         hl[k] = s - ph[k] * a.heads_per_cta;
     }
     const int iters = a.stage_pos / a.phases;
+    const uint32_t consumer_threads = static_cast<uint32_t>(a.active_warps) * 32;
     float *mbuf = reinterpret_cast<float *>(smem + a.merge_offset);
     const int rec = D + 2;
     int st = 0;
@@ -488,9 +491,9 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                     }
                 }
             }
-            named_barrier_sync(1, kConsumerThreads);
+            named_barrier_sync(1, consumer_threads);
             const bool all_write = !*abort_flag;  // same for every consumer after the barrier
-            for (int idx = threadIdx.x; all_write && idx < hg * D; idx += kConsumerThreads) {
+            for (int idx = threadIdx.x; all_write && idx < hg * D; idx += consumer_threads) {
                 const int h = idx / D;
                 const int d = idx - h * D;
                 float M = -INFINITY;
@@ -515,7 +518,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                     if (d == 0) a.ws_ml[row] = make_float2(M, lsum);
                 }
             }
-            named_barrier_sync(1, kConsumerThreads);
+            named_barrier_sync(1, consumer_threads);
         }
     }
 }
