@@ -97,38 +97,45 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
     float M = -INFINITY, L = 0.f;
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
     if (sub < nsub) {
-        int j = sub;
-        for (; j + 3 * nsub < npieces; j += 4 * nsub) {
-            float2 ml[4];
-            float4 v[4];
+        // issue the loads of up to eight pieces before folding any of them
+        for (int j0 = sub; j0 < npieces; j0 += 8 * nsub) {
+            float2 ml[8];
+            float4 v[8];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const size_t row = static_cast<size_t>(piece_slot(c_first + j + r * nsub, u)) * hgs + hl;
-                ml[r] = a.ws_ml[row];
-                v[r] = *reinterpret_cast<const float4 *>(a.ws_acc + row * a.D + c0 + f * 4);
+            for (int r = 0; r < 8; ++r) {
+                const int j = j0 + r * nsub;
+                ml[r] = make_float2(-INFINITY, 0.f);
+                v[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (j < npieces) {
+                    const size_t row = static_cast<size_t>(piece_slot(c_first + j, u)) * hgs + hl;
+                    ml[r] = a.ws_ml[row];
+                    v[r] = *reinterpret_cast<const float4 *>(a.ws_acc + row * a.D + c0 + f * 4);
+                }
             }
 #pragma unroll
-            for (int r = 0; r < 4; ++r) fold(M, L, A, ml[r].x, ml[r].y, v[r]);
-        }
-        for (; j < npieces; j += nsub) {
-            const size_t row = static_cast<size_t>(piece_slot(c_first + j, u)) * hgs + hl;
-            const float2 ml = a.ws_ml[row];
-            const float4 v = *reinterpret_cast<const float4 *>(a.ws_acc + row * a.D + c0 + f * 4);
-            fold(M, L, A, ml.x, ml.y, v);
+            for (int r = 0; r < 8; ++r) fold(M, L, A, ml[r].x, ml[r].y, v[r]);
         }
     }
     sm_m[tid] = M;
     sm_l[tid] = L;
     sm_a[tid] = A;
     __syncthreads();
-    if (tid < f4) {
-        float M2 = -INFINITY, L2 = 0.f;
-        float4 A2 = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int r = 0; r < nsub; ++r) {
-            const int t = r * f4 + tid;
-            fold(M2, L2, A2, sm_m[t], sm_l[t], sm_a[t]);
+    // tree fold over the pieces-in-flight index, for each float4 lane
+    for (int step = 1; step < nsub; step <<= 1) {
+        if (sub < nsub && (sub % (2 * step)) == 0 && sub + step < nsub) {
+            const int t = tid, o = tid + step * f4;
+            float m2 = sm_m[t], l2 = sm_l[t];
+            float4 a2 = sm_a[t];
+            fold(m2, l2, a2, sm_m[o], sm_l[o], sm_a[o]);
+            sm_m[t] = m2;
+            sm_l[t] = l2;
+            sm_a[t] = a2;
         }
-        const float inv = 1.f / L2;
+        __syncthreads();
+    }
+    if (tid < f4) {
+        const float4 A2 = sm_a[tid];
+        const float inv = 1.f / sm_l[tid];
         __half2 lo = __floats2half2_rn(A2.x * inv, A2.y * inv);
         __half2 hi = __floats2half2_rn(A2.z * inv, A2.w * inv);
         uint2 packed;

@@ -37,6 +37,7 @@ constexpr int kStageTargetBytesOnePerSm = 40 * 1024;  // K+V per stage, 1 CTA/SM
 constexpr int kTwoPerSmBudget = 110 * 1024;  // ring bytes per CTA at 2 CTAs/SM
 constexpr int kOnePerSmBudget = 200 * 1024;  // ring bytes per CTA at 1 CTA/SM
 constexpr int kMaxStages = 12;
+constexpr long long kDeepRingPositions = 64;  // per CTA, below which the deep ring is used
 constexpr int kStaticSmemReserve = 1024;  // the decode kernel's static shared memory
 
 thread_local std::string g_last_error;
@@ -201,9 +202,13 @@ int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
     p.P = P;
     const int stage_bytes = 2 * P * row_bytes;
     const int merge_bytes = p.PHI > 1 ? p.HG * p.PHI * (D + 2) * 4 : 0;
-    const int ring_budget = dattn::decode_min_blocks(nwc) == 2
-                                ? kTwoPerSmBudget - merge_bytes
-                                : kOnePerSmBudget - merge_bytes;
+    // Two CTAs per SM when the batch gives every one of them a long range;
+    // otherwise one CTA per SM with a ring twice as deep, so a CTA keeps enough
+    // bytes in flight on its own (a small batch cannot fill two per SM).
+    const long long capacity_pos = static_cast<long long>(B) * p.NHG * S;
+    const bool deep = dattn::decode_min_blocks(nwc) == 1 ||
+                      capacity_pos < kDeepRingPositions * 2LL * di.sms;
+    const int ring_budget = deep ? kOnePerSmBudget - merge_bytes : kTwoPerSmBudget - merge_bytes;
     int nst = ring_budget / stage_bytes;
     if (nst < 2) nst = (di.max_smem_optin - 1024 - merge_bytes) / stage_bytes;
     p.NST = std::max(2, std::min(kMaxStages, nst));
