@@ -28,16 +28,38 @@ using dattn::DecodeVariant;
 
 constexpr int kVersion = 10000;        // 1.0.0
 constexpr int kMaxPartitions = 65535;  // CTAs of the decode grid
-constexpr long long kMinPositions = 16;  // positions per partition chosen by the library
 constexpr int kMaxHeadDim = 256;
 constexpr int kMaxHeadsPerLaneGroup = 4;  // register slots per lane group (KMAX)
 constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
-constexpr int kStageTargetBytes = 32 * 1024;          // K+V per stage, 2 CTAs/SM
-constexpr int kStageTargetBytesOnePerSm = 40 * 1024;  // K+V per stage, 1 CTA/SM
-constexpr int kTwoPerSmBudget = 110 * 1024;  // ring bytes per CTA at 2 CTAs/SM
-constexpr int kOnePerSmBudget = 200 * 1024;  // ring bytes per CTA at 1 CTA/SM
+// Tiling constants of the plan.  Each can be overridden at compile time
+// (-DDATTN_<NAME>=value) to explore other configurations.
+#ifndef DATTN_STAGE_BYTES_TWO_PER_SM
+#define DATTN_STAGE_BYTES_TWO_PER_SM (32 * 1024)
+#endif
+#ifndef DATTN_STAGE_BYTES_ONE_PER_SM
+#define DATTN_STAGE_BYTES_ONE_PER_SM (40 * 1024)
+#endif
+#ifndef DATTN_RING_BYTES_TWO_PER_SM
+#define DATTN_RING_BYTES_TWO_PER_SM (110 * 1024)
+#endif
+#ifndef DATTN_RING_BYTES_ONE_PER_SM
+#define DATTN_RING_BYTES_ONE_PER_SM (200 * 1024)
+#endif
+#ifndef DATTN_DEEP_RING_POSITIONS
+#define DATTN_DEEP_RING_POSITIONS 64
+#endif
+#ifndef DATTN_MIN_POSITIONS
+#define DATTN_MIN_POSITIONS 16
+#endif
+constexpr int kStageTargetBytes = DATTN_STAGE_BYTES_TWO_PER_SM;         // K+V per stage, 2 CTAs/SM
+constexpr int kStageTargetBytesOnePerSm = DATTN_STAGE_BYTES_ONE_PER_SM;  // K+V per stage, 1 CTA/SM
+constexpr int kTwoPerSmBudget = DATTN_RING_BYTES_TWO_PER_SM;  // ring bytes per CTA at 2 CTAs/SM
+constexpr int kOnePerSmBudget = DATTN_RING_BYTES_ONE_PER_SM;  // ring bytes per CTA at 1 CTA/SM
 constexpr int kMaxStages = 12;
-constexpr long long kDeepRingPositions = 64;  // per CTA, below which the deep ring is used
+// positions per CTA at two CTAs per SM below which one CTA per SM with a deep
+// ring is used
+constexpr long long kDeepRingPositions = DATTN_DEEP_RING_POSITIONS;
+constexpr long long kMinPositions = DATTN_MIN_POSITIONS;  // per partition chosen by the library
 constexpr int kStaticSmemReserve = 1024;  // the decode kernel's static shared memory
 
 thread_local std::string g_last_error;
@@ -196,18 +218,18 @@ int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
     // warps whose first lane group holds a slot (slot s = lane group + k * nlg)
     p.active_warps = std::min(nwc, (p.HG * p.PHI + (32 / bdx) - 1) / (32 / bdx));
     const int row_bytes = p.HG * D * 2;
-    const int stage_target = nwc == 8 ? kStageTargetBytes : kStageTargetBytesOnePerSm;
-    int P = std::max(1, std::min(256, stage_target / 2 / row_bytes));
-    P = std::max(p.PHI, P / p.PHI * p.PHI);
-    p.P = P;
-    const int stage_bytes = 2 * P * row_bytes;
-    const int merge_bytes = p.PHI > 1 ? p.HG * p.PHI * (D + 2) * 4 : 0;
     // Two CTAs per SM when the batch gives every one of them a long range;
     // otherwise one CTA per SM with a ring twice as deep, so a CTA keeps enough
     // bytes in flight on its own (a small batch cannot fill two per SM).
     const long long capacity_pos = static_cast<long long>(B) * p.NHG * S;
     const bool deep = dattn::decode_min_blocks(nwc) == 1 ||
                       capacity_pos < kDeepRingPositions * 2LL * di.sms;
+    const int stage_target = deep ? kStageTargetBytesOnePerSm : kStageTargetBytes;
+    int P = std::max(1, std::min(256, stage_target / 2 / row_bytes));
+    P = std::max(p.PHI, P / p.PHI * p.PHI);
+    p.P = P;
+    const int stage_bytes = 2 * P * row_bytes;
+    const int merge_bytes = p.PHI > 1 ? p.HG * p.PHI * (D + 2) * 4 : 0;
     const int ring_budget = deep ? kOnePerSmBudget - merge_bytes : kTwoPerSmBudget - merge_bytes;
     int nst = ring_budget / stage_bytes;
     if (nst < 2) nst = (di.max_smem_optin - 1024 - merge_bytes) / stage_bytes;
