@@ -37,7 +37,7 @@ constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
 #define DATTN_STAGE_BYTES_TWO_PER_SM (32 * 1024)
 #endif
 #ifndef DATTN_STAGE_BYTES_ONE_PER_SM
-#define DATTN_STAGE_BYTES_ONE_PER_SM (40 * 1024)
+#define DATTN_STAGE_BYTES_ONE_PER_SM (64 * 1024)
 #endif
 #ifndef DATTN_RING_BYTES_TWO_PER_SM
 #define DATTN_RING_BYTES_TWO_PER_SM (110 * 1024)
@@ -46,7 +46,7 @@ constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
 #define DATTN_RING_BYTES_ONE_PER_SM (200 * 1024)
 #endif
 #ifndef DATTN_DEEP_RING_POSITIONS
-#define DATTN_DEEP_RING_POSITIONS 64
+#define DATTN_DEEP_RING_POSITIONS (1LL << 40)
 #endif
 #ifndef DATTN_MIN_POSITIONS
 #define DATTN_MIN_POSITIONS 16
@@ -218,9 +218,10 @@ int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
     // warps whose first lane group holds a slot (slot s = lane group + k * nlg)
     p.active_warps = std::min(nwc, (p.HG * p.PHI + (32 / bdx) - 1) / (32 / bdx));
     const int row_bytes = p.HG * D * 2;
-    // Two CTAs per SM when the batch gives every one of them a long range;
-    // otherwise one CTA per SM with a ring twice as deep, so a CTA keeps enough
-    // bytes in flight on its own (a small batch cannot fill two per SM).
+    // One CTA per SM with a deep ring of large stages (measured best on GB300
+    // for every workload shape: a CTA alone keeps ~190 KB in flight, and large
+    // bulk copies are the most efficient).  Two CTAs per SM with half the ring
+    // remain available through DATTN_DEEP_RING_POSITIONS.
     const long long capacity_pos = static_cast<long long>(B) * p.NHG * S;
     const bool deep = dattn::decode_min_blocks(nwc) == 1 ||
                       capacity_pos < kDeepRingPositions * 2LL * di.sms;
