@@ -19,6 +19,7 @@
 
 using dattn::piece_slot;
 using dattn::range_begin;
+using dattn::range_begin_split;
 using dattn::range_owner;
 
 static int fail(const char *what, long long a, long long b) {
@@ -47,6 +48,12 @@ int main() {
             for (long long c = 0; c < G; ++c) {
                 const long long n = range_begin(c + 1, W, G) - range_begin(c, W, G);
                 if (n < W / G || n > W / G + 1) return fail("balance", c, n);
+            }
+            for (long long c = 0; c <= G; ++c) {
+                if (range_begin_split(static_cast<unsigned>(c), W / G,
+                                      static_cast<unsigned>(W % G),
+                                      static_cast<unsigned>(G)) != range_begin(c, W, G))
+                    return fail("split begin", c, G);
             }
             // owner of every position
             for (long long x = 0; x < W; ++x) {
@@ -89,6 +96,15 @@ int main() {
                 }
             }
         }
+    }
+    // the 32-bit split form at the largest partition counts and big W
+    for (int trial = 0; trial < 200000; ++trial) {
+        const long long G = 1 + static_cast<long long>(rng() % 65535);
+        const long long W = static_cast<long long>(rng() % (1ULL << 40)) + 1;
+        const long long c = static_cast<long long>(rng() % (G + 1));
+        if (range_begin_split(static_cast<unsigned>(c), W / G, static_cast<unsigned>(W % G),
+                              static_cast<unsigned>(G)) != range_begin(c, W, G))
+            return fail("split begin (large)", c, G);
     }
     std::printf("streamk partition checks passed\n");
     return 0;

@@ -32,6 +32,7 @@ namespace dattn {
 namespace {
 
 constexpr int kThreads = 128;
+constexpr int kInlinePrefix = 4096;  // batches summed from current_pos in the combine
 
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -60,9 +61,15 @@ __device__ __forceinline__ void fold(float &M, float &L, float4 &A, float m, flo
     A.w = fmaf(w, a.w, A.w);
 }
 
+__device__ __forceinline__ long long live_len(const uint32_t *cp, long long b, int S) {
+    const uint32_t c = __ldg(cp + b);
+    return c >= static_cast<uint32_t>(S - 1) ? S : static_cast<long long>(c) + 1;
+}
+
 __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) {
     __shared__ float sm_m[kThreads], sm_l[kThreads];
     __shared__ float4 sm_a[kThreads];
+    __shared__ long long sm_pre[kThreads / 32][2];
 
     const int nchunks = (a.D + a.chunk - 1) / a.chunk;
     const long long idx = blockIdx.x;
@@ -74,19 +81,50 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
     const int hl = h - g * a.heads_per_cta;
     const long long u = b * a.head_groups + g;
 
-    const uint32_t cp = __ldg(a.cur_pos + b);
-    const long long Lb = cp >= static_cast<uint32_t>(a.S - 1) ? a.S : static_cast<long long>(cp) + 1;
+    const int tid = threadIdx.x;
+    const long long Lb = live_len(a.cur_pos, b, a.S);
+    // Live positions before sequence b and in total.  For batches of up to
+    // kInlinePrefix sequences they are summed here from current_pos (an input,
+    // readable before the decode kernel finishes); larger batches read the
+    // prefix sums the decode kernel wrote.
+    long long before = 0, total = 0;
+    if (a.B <= kInlinePrefix) {
+        for (int i = tid; i < a.B; i += kThreads) {
+            const long long L = live_len(a.cur_pos, i, a.S);
+            total += L;
+            if (i < b) before += L;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            before += __shfl_xor_sync(0xffffffffu, before, o);
+            total += __shfl_xor_sync(0xffffffffu, total, o);
+        }
+        if ((tid & 31) == 0) {
+            sm_pre[tid >> 5][0] = before;
+            sm_pre[tid >> 5][1] = total;
+        }
+        __syncthreads();
+        before = total = 0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) {
+            before += sm_pre[w][0];
+            total += sm_pre[w][1];
+        }
+    }
 
     pdl_wait_primary();  // the decode kernel's workspace writes are visible after this
+    if (a.B > kInlinePrefix) {
+        before = a.ws_prefix[b];
+        total = a.ws_prefix[a.B];
+    }
     const long long nhg = a.head_groups;
-    const long long W = nhg * a.ws_prefix[a.B];
-    const long long Pu = nhg * a.ws_prefix[b] + g * Lb;
+    const long long W = nhg * total;
+    const long long Pu = nhg * before + g * Lb;
     const long long c_first = range_owner(Pu, W, a.partitions);
     const long long c_last = range_owner(Pu + Lb - 1, W, a.partitions);
     if (c_first == c_last) return;  // written whole by the decode kernel
     const int npieces = static_cast<int>(c_last - c_first + 1);
 
-    const int tid = threadIdx.x;
     const int c0 = chunk * a.chunk;
     const int width = min(a.chunk, a.D - c0);  // a multiple of 8
     const int f4 = width / 4;                  // float4 per piece row

@@ -250,6 +250,8 @@ int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
     // partition arithmetic multiplies a partition index by the flattened
     // position count: keep it inside 64 bits
     const double capacity = static_cast<double>(B) * p.NHG * S;
+    if (static_cast<double>(p.NHG) * S >= 2147483648.0)
+        return fail(DATTN_ERR_UNSUPPORTED, "head_groups x seq_len must stay below 2^31");
     if (capacity * (p.G + 1.0) > 4.0e18)
         return fail(DATTN_ERR_UNSUPPORTED, "batch of %.3g positions is too large", capacity);
     if (p.G > 1) {

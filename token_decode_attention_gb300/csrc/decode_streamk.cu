@@ -142,9 +142,10 @@ __device__ __forceinline__ bool next_piece(Walker &w, const DecodeArgs &a) {
         ++w.b;
         w.Lb = live_len(a.cur_pos, w.b, a.S);
     }
-    const long long rel = w.x - w.base;
-    w.g = static_cast<int>(rel / w.Lb);
-    w.off = static_cast<int>(rel - static_cast<long long>(w.g) * w.Lb);
+    // rel < head_groups * seq_len < 2^31 (checked by the host): 32-bit division
+    const unsigned rel = static_cast<unsigned>(w.x - w.base);
+    w.g = static_cast<int>(rel / static_cast<unsigned>(w.Lb));
+    w.off = static_cast<int>(rel - static_cast<unsigned>(w.g) * static_cast<unsigned>(w.Lb));
     const long long rest = w.x1 - w.x;
     w.len = static_cast<int>(rest < w.Lb - w.off ? rest : w.Lb - w.off);
     w.u = w.b * nhg + w.g;
@@ -204,8 +205,11 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     const long long excl = before + incl - sum;
     const long long nhg = a.head_groups;
     const long long W = total * nhg;
-    const long long x0 = range_begin(blockIdx.x, W, a.partitions);
-    const long long x1 = range_begin(static_cast<long long>(blockIdx.x) + 1, W, a.partitions);
+    const unsigned G = static_cast<unsigned>(a.partitions);
+    const long long wq = W / G;
+    const unsigned wr = static_cast<unsigned>(W - wq * G);
+    const long long x0 = range_begin_split(blockIdx.x, wq, wr, G);
+    const long long x1 = range_begin_split(blockIdx.x + 1, wq, wr, G);
     if (x0 < x1 && nhg * excl <= x0 && x0 < nhg * (excl + sum)) {
         long long run = excl;
         for (long long b = bb; b < be; ++b) {

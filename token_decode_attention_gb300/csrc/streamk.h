@@ -32,6 +32,14 @@ DATTN_HD long long range_owner(long long x, long long W, long long G) {
     return ((x + 1) * G + W - 1) / W - 1;
 }
 
+// range_begin(c, W, G) with W = wq * G + wr (wq = W / G, wr = W % G) and
+// G <= 65535: c * W / G = c * wq + (c * wr) / G exactly, and c * wr < G * G
+// fits in 32 bits, so the per-partition division is a 32-bit one.
+DATTN_HD long long range_begin_split(unsigned c, long long wq, unsigned wr, unsigned G) {
+    return static_cast<long long>(c) * wq +
+           static_cast<long long>(static_cast<unsigned>(static_cast<unsigned long long>(c) * wr) / G);
+}
+
 // Workspace slot of the piece of unit u processed by partition c.
 DATTN_HD long long piece_slot(long long c, long long u) { return c + u; }
 
