@@ -68,7 +68,8 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per call from a committed ncu summary, if it matches these sources."""
+    """DRAM bytes per call of the decode kernel from a committed ncu capture
+    (profiles/ncu_traffic.json), if it was taken on these kernel sources."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -471,7 +472,8 @@ def main():
         "roofline": {"bound": "hbm", "achieved": per_call, "peak": peak, "unit": "GB/s",
                      "frac": per_call / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "traffic": recorded_traffic(w.name),
-                     "kernel": "dattn_decode_f16_ex call: decode_splitk_kernel + combine_kernel",
+                     "kernel": "one dattn_decode_f16_ex call: decode_streamk_kernel "
+                               "(dominant) + combine_kernel launched with PDL",
                      "algorithmic_bytes_per_call": rep.bytes_per_step},
         "e2e": e2e,
         "submission": "eager Python calls" if args.eager else
