@@ -154,6 +154,32 @@ def barrier(world: int):
         dist.barrier()
 
 
+def whole_job(ms_local: float, steps: int, bytes_per_step_local: int, heads_per_step_local: int,
+              world: int, device) -> dict:
+    """Aggregate one replica's timing into the whole-job figures.
+
+    Every rank runs its own replica (weak scaling); the job takes as long as
+    the slowest rank, and the work is the sum over ranks.  Collective on every
+    rank when world > 1.
+    """
+    ms_max = max_over_ranks(ms_local, world, device)
+    t_step = ms_max * 1e-3 / steps
+    total_bytes = all_ranks_sum(bytes_per_step_local, world, device)
+    total_heads = all_ranks_sum(heads_per_step_local, world, device)
+    return {"ms_per_step": ms_max / steps, "t_step": t_step,
+            "value_gbs": total_bytes / t_step / 1e9, "query_heads_per_s": total_heads / t_step,
+            "total_bytes_per_step": total_bytes}
+
+
+def all_ranks_sum(x: int, world: int, device) -> int:
+    if world == 1:
+        return int(x)
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return int(t.item())
+
+
 # ------------------------------------------------------------- our arm
 
 class Replica:
@@ -441,10 +467,10 @@ def main():
                            graph=not args.eager)
     eager_ms, _ = rep.timed(args.steps, 1, stream, world, soak_s=0.0, graph=False)
     eager_ms = max_over_ranks(eager_ms, world, device)
-    ms_max = max_over_ranks(ms, world, device)
-    t_step = ms_max * 1e-3 / args.steps
-    total_bytes = rep.bytes_per_step * world
-    value = total_bytes / t_step / 1e9
+    job = whole_job(ms, args.steps, rep.bytes_per_step, rep.w.batch * rep.w.n_heads, world,
+                    device)
+    t_step = job["t_step"]
+    value = job["value_gbs"]
     per_call = rep.bytes_per_step / t_step / 1e9
     e2e = rep.e2e(args.steps, args.warmup, stream)
     if dattn.dattn_device_error(clear=True) != 0:
@@ -467,7 +493,7 @@ def main():
                    "current_pos": "per-sequence" if w.current_pos is None else w.current_pos,
                    "partitions": rep.plan["partitions"], "l2": rep.l2_note,
                    "parallelism": f"replicas x{world}"},
-        "query_heads_per_s": world * w.batch * w.n_heads / t_step,
+        "query_heads_per_s": job["query_heads_per_s"],
         "frac_of_nominal_8TBs": per_call / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": per_call, "peak": peak, "unit": "GB/s",
                      "frac": per_call / peak, "peak_source": f"{peak_kind} hbm_gbs",

@@ -219,6 +219,17 @@ int dattn_decode_f16_noalloc(const void *Q, const void *K_cache, const void *V_c
  */
 int dattn_device_error(int clear);
 
+/*
+ * Self-test of the failure detection above (no counterpart on the pages).
+ * Enqueues on `stream` one CTA that waits, with the same bounded wait the
+ * decode kernel uses, on an mbarrier nothing ever arrives on.  After about one
+ * second the wait runs out, the CTA records a code in the device error word and
+ * returns; no fault, trap or hang is involved and the context stays usable.  A
+ * following dattn_device_error() then returns DATTN_ERR_TIMEOUT.
+ * Errors: CUDA.
+ */
+int dattn_selftest_wait_timeout(dattn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

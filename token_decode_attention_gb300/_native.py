@@ -56,6 +56,7 @@ _SIGNATURES = {
     "dattn_qk_f16": ([_P, _P, _P, _I, _I, _I, _I, _P, _P], _I),
     "dattn_pv_f16": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
     "dattn_device_error": ([_I], _I),
+    "dattn_selftest_wait_timeout": ([_P], _I),
 }
 
 
@@ -199,6 +200,11 @@ def dattn_device_error(clear: bool = True) -> int:
     if st not in (OK, ERR_TIMEOUT):
         _check(st, "dattn_device_error")
     return st
+
+
+def dattn_selftest_wait_timeout(stream=None) -> None:
+    _check(load().dattn_selftest_wait_timeout(_stream_handle(stream)),
+           "dattn_selftest_wait_timeout")
 
 
 # ------------------------------------------------------- convenience forms

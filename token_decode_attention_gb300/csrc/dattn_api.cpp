@@ -487,6 +487,14 @@ int dattn_pv_f16(const void *scores, const void *V_cache, void *out, int batch, 
     return e == cudaSuccess ? DATTN_OK : fail_cuda(e, "pv kernel launch");
 }
 
+int dattn_selftest_wait_timeout(dattn_stream_t stream) {
+    DeviceInfo di;
+    if (int st = device_info(&di)) return st;
+    const cudaError_t e =
+        dattn::launch_wait_timeout_selftest(di.err_word, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DATTN_OK : fail_cuda(e, "self-test kernel launch");
+}
+
 int dattn_device_error(int clear) {
     DeviceInfo di;
     if (int st = device_info(&di)) return st;

@@ -18,6 +18,10 @@ __host__ __device__ constexpr int decode_min_blocks(int nwc) { return nwc <= 8 ?
 constexpr unsigned kErrConsumerWait = 1u;
 constexpr unsigned kErrProducerWait = 2u;
 constexpr unsigned kErrDrainWait = 4u;
+constexpr unsigned kErrSelftestWait = 8u;
+
+// Time limit of every pipeline wait in the library's kernels.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // one second
 
 // Arguments of the stream-K decode kernel.
 //
@@ -86,6 +90,10 @@ cudaError_t device_error_word(unsigned **ptr);
 // Record `message` as the calling thread's dattn_last_error() text and return
 // `status` (for entry points defined outside dattn_api.cpp).
 int set_last_error(int status, const char *message);
+
+// Failure-detection self-test: one CTA waits (bounded) on an mbarrier that
+// nothing arrives on and records kErrSelftestWait in `err` when the wait runs out.
+cudaError_t launch_wait_timeout_selftest(unsigned *err, cudaStream_t stream);
 
 // Page-faithful split calls.
 cudaError_t launch_qk(const void *Q, const void *K, void *scores, int B, int H, int D, int S,

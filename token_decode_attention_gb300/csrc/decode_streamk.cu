@@ -48,16 +48,10 @@ __device__ unsigned g_device_error = 0;
 
 namespace {
 
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per wait
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-    }
-    return true;
+    return mbar_wait_bounded(bar, parity, kWaitLimitNs);
 }
 
 __device__ __forceinline__ int live_len(const uint32_t *cp, long long b, int S) {

@@ -60,6 +60,20 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// Wait for the phase with the given parity to complete, giving up after
+// `limit_ns` of global time.  Returns false when the wait ran out.  Every
+// pipeline wait in this library goes through here, so no kernel can hang on a
+// barrier that is never completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
+}
+
 // L2 policy for data read exactly once: evict first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t pol;
