@@ -40,6 +40,9 @@ def _load(path: str):
     lib.oracle_f16_to_f64_array.argtypes = [u16p, f64p, i64]
     lib.oracle_f32_to_f16_array.argtypes = [ctypes.POINTER(ctypes.c_float), u16p, i64]
     lib.oracle_max_threads.restype = ctypes.c_int
+    lib.oracle_decode_paged_f64.argtypes = [u16p, u16p, u16p, i64, i64, i64, i64, i64,
+                                            ctypes.POINTER(ctypes.c_int32), i64, u32p, f64p,
+                                            ctypes.c_int]
     return lib
 
 
@@ -97,6 +100,34 @@ def decode_f64(Q, K, V, current_pos, threads: int = 0) -> np.ndarray:
     _lib().oracle_decode_f64(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
                              _ptr(v, ctypes.c_uint16), B, H, D, S,
                              _ptr(cp, ctypes.c_uint32), _ptr(out, ctypes.c_double), threads)
+    return out
+
+
+def decode_paged_f64(Q, K_pages, V_pages, block_table, current_pos,
+                     threads: int = 0) -> np.ndarray:
+    """Fused decode attention over a paged cache, fp64.
+
+    Q [B,H,D], K/V pages [num_pages, page_size, H, D] float16, block_table
+    [B, max_pages] int32, current_pos [B] -> out [B,H,D] float64 (NaN rows for
+    sequences whose live pages are not valid indices).
+    """
+    q = _f16_bits(Q, 3, "Q")
+    kp = _f16_bits(K_pages, 4, "K_pages")
+    vp = _f16_bits(V_pages, 4, "V_pages")
+    B, H, D = q.shape
+    num_pages, page_size = kp.shape[0], kp.shape[1]
+    if kp.shape != (num_pages, page_size, H, D) or vp.shape != kp.shape:
+        raise ValueError(f"page shapes {kp.shape}/{vp.shape} do not match Q {q.shape}")
+    table = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    if table.ndim != 2 or table.shape[0] != B:
+        raise ValueError(f"block_table must be [{B}, max_pages], got {table.shape}")
+    cp = _cur_pos(current_pos, B)
+    out = np.empty((B, H, D), dtype=np.float64)
+    _lib().oracle_decode_paged_f64(_ptr(q, ctypes.c_uint16), _ptr(kp, ctypes.c_uint16),
+                                   _ptr(vp, ctypes.c_uint16), B, H, D, page_size,
+                                   table.shape[1], _ptr(table, ctypes.c_int32), num_pages,
+                                   _ptr(cp, ctypes.c_uint32), _ptr(out, ctypes.c_double),
+                                   threads)
     return out
 
 

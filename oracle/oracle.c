@@ -157,6 +157,70 @@ void oracle_decode_f64(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
 }
 
 /*
+ * Decode attention over a paged KV cache, fp64.  The cache holds pages of
+ * page_size positions: K_pages / V_pages [num_pages, page_size, H, D].  Position
+ * p of sequence b lives in page table[b * max_pages + p / page_size] at row
+ * p % page_size, so the logical cache of sequence b is
+ *   K[b, p, h, :] = K_pages[table[b, p / page_size], p % page_size, h, :]
+ * with capacity S = page_size * max_pages.  Everything else is the fused
+ * computation above (same live length, scores, softmax and weighted sum).
+ * Page indices outside [0, num_pages) are not read: the affected sequence's
+ * output is set to NaN, which no valid result equals.
+ */
+void oracle_decode_paged_f64(const uint16_t *Q, const uint16_t *K_pages,
+                             const uint16_t *V_pages, int64_t B, int64_t H, int64_t D,
+                             int64_t page_size, int64_t max_pages, const int32_t *table,
+                             int64_t num_pages, const uint32_t *current_pos, double *out,
+                             int nthreads) {
+    set_threads(nthreads);
+    const int64_t S = page_size * max_pages;
+    const double inv_sqrt_d = 1.0 / sqrt((double)D);
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)S);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t bh = 0; bh < B * H; ++bh) {
+            const int64_t b = bh / H, h = bh % H;
+            const int64_t L = live_length(current_pos[b], S);
+            const uint16_t *q = Q + (b * H + h) * D;
+            double *o = out + (b * H + h) * D;
+            int bad = 0;
+            for (int64_t p = 0; p < L; ++p) {
+                const int64_t pg = table[b * max_pages + p / page_size];
+                if (pg < 0 || pg >= num_pages) bad = 1;
+            }
+            if (bad) {
+                for (int64_t d = 0; d < D; ++d) o[d] = NAN;
+                continue;
+            }
+            double M = -INFINITY;
+            for (int64_t p = 0; p < L; ++p) {
+                const int64_t pg = table[b * max_pages + p / page_size];
+                const uint16_t *k = K_pages + ((pg * page_size + p % page_size) * H + h) * D;
+                double dot = 0.0;
+                for (int64_t i = 0; i < D; ++i)
+                    dot += oracle_f16_to_f64(q[i]) * oracle_f16_to_f64(k[i]);
+                s[p] = dot * inv_sqrt_d;
+                if (s[p] > M) M = s[p];
+            }
+            double den = 0.0;
+            for (int64_t p = 0; p < L; ++p) {
+                s[p] = exp(s[p] - M);
+                den += s[p];
+            }
+            for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+            for (int64_t p = 0; p < L; ++p) {
+                const int64_t pg = table[b * max_pages + p / page_size];
+                const uint16_t *v = V_pages + ((pg * page_size + p % page_size) * H + h) * D;
+                const double w = s[p] / den;
+                for (int64_t d = 0; d < D; ++d) o[d] += w * oracle_f16_to_f64(v[d]);
+            }
+        }
+        free(s);
+    }
+}
+
+/*
  * The QK step in fp64: scores[b,h,p] = (Q[b,h,:] . K[b,p,h,:]) / sqrt(D) for
  * p <= cp_b, exactly -infinity for p > cp_b (kernel attention_qk_f16).  All S
  * positions are produced, like the page's [n_heads, seq_len] scores buffer.

@@ -44,6 +44,10 @@ MUTANTS = [
     ("qk_pages_no_scale", "score = score * scale;", "", 1),
     ("pv_no_normalisation", "const double wp = w[p] / den;", "const double wp = w[p];", 1),
     ("pv_no_max", "if (s > M) M = s;", "", 1),
+    ("paged_row_offset", "const uint16_t *k = K_pages + ((pg * page_size + p % page_size) * H + h) * D;",
+     "const uint16_t *k = K_pages + ((pg * page_size + p / page_size) * H + h) * D;", 1),
+    ("paged_v_page_of_k", "const uint16_t *v = V_pages + ((pg * page_size + p % page_size) * H + h) * D;",
+     "const uint16_t *v = V_pages + ((pg + p % page_size) * H + h) * D;", 1),
     ("pv_v_transposed", "const uint16_t *v = V + ((b * S + p) * H + h) * D;\n"
      "                const double wp",
      "const uint16_t *v = V + ((b * H + h) * S + p) * D;\n                const double wp", 1),
@@ -67,6 +71,8 @@ def _pin_checks():
         ("page_single_channel", pins.test_page_qk_single_channel_is_one_rounded_product),
         ("pv_closed", pins.test_pv_closed_forms),
         ("qk_square", pins.test_qk_f64_square_head_dims_exact),
+        ("paged_identity", pins.test_paged_identity_table_equals_dense),
+        ("paged_random", lambda: pins.test_paged_random_and_shared_tables_equal_dense_gather(5)),
     ]
 
 

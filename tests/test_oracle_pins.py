@@ -342,3 +342,78 @@ def test_qk_f64_square_head_dims_exact():
                 exact = sum(Fraction(float(Q[0, h, i])) * Fraction(float(K[0, p, h, i]))
                             for i in range(D)) / r
                 assert abs(got[0, h, p] - float(exact)) <= 1e-14 * max(1.0, abs(float(exact)))
+
+
+# --------------------------------------------------------- paged KV cache
+
+def _paged_case(rng, B, H, D, ps, maxp, extra_pages=3, share=False):
+    num_pages = B * maxp + extra_pages
+    Kp = rand_f16(rng, (num_pages, ps, H, D))
+    Vp = rand_f16(rng, (num_pages, ps, H, D))
+    table = rng.permutation(num_pages)[: B * maxp].reshape(B, maxp).astype(np.int32)
+    if share and B > 1:
+        table[1, :2] = table[0, :2]  # a shared prefix: two sequences read the same pages
+    return Kp, Vp, table
+
+
+def _gather_dense(pages, table, ps):
+    # the logical cache K[b, p] = pages[table[b, p // ps], p % ps] (numpy indexing)
+    B, maxp = table.shape
+    p = np.arange(maxp * ps)
+    return pages[table[:, p // ps], p % ps]          # [B, S, H, D]
+
+
+def test_paged_identity_table_equals_dense():
+    rng = np.random.default_rng(40)
+    B, H, D, ps, maxp = 3, 4, 32, 8, 6
+    S = ps * maxp
+    Q, K, V = rand_f16(rng, (B, H, D)), rand_f16(rng, (B, S, H, D)), rand_f16(rng, (B, S, H, D))
+    Kp = K.reshape(B * maxp, ps, H, D)
+    Vp = V.reshape(B * maxp, ps, H, D)
+    table = np.arange(B * maxp, dtype=np.int32).reshape(B, maxp)
+    cp = np.array([47, 9, 0], np.uint32)
+    assert np.array_equal(oracle.decode_paged_f64(Q, Kp, Vp, table, cp),
+                          oracle.decode_f64(Q, K, V, cp))
+
+
+@pytest.mark.parametrize("ps", [1, 5, 16])
+def test_paged_random_and_shared_tables_equal_dense_gather(ps):
+    rng = np.random.default_rng(41 + ps)
+    B, H, D, maxp = 4, 3, 16, 7
+    Kp, Vp, table = _paged_case(rng, B, H, D, ps, maxp, share=True)
+    Q = rand_f16(rng, (B, H, D))
+    cp = np.array([ps * maxp - 1, 3, ps * maxp + 100, 0], np.uint32)
+    dense = oracle.decode_f64(Q, _gather_dense(Kp, table, ps), _gather_dense(Vp, table, ps), cp)
+    assert np.array_equal(oracle.decode_paged_f64(Q, Kp, Vp, table, cp), dense)
+
+
+def test_paged_unreferenced_and_past_live_pages_do_not_matter():
+    rng = np.random.default_rng(45)
+    B, H, D, ps, maxp = 2, 2, 8, 4, 5
+    Kp, Vp, table = _paged_case(rng, B, H, D, ps, maxp, extra_pages=4)
+    Q = rand_f16(rng, (B, H, D))
+    cp = np.array([5, 10], np.uint32)  # live pages: 0..1 and 0..2
+    base = oracle.decode_paged_f64(Q, Kp, Vp, table, cp)
+    used = set(table[0, :2].tolist()) | set(table[1, :3].tolist())
+    Kp2, Vp2 = Kp.copy(), Vp.copy()
+    for pg in range(Kp.shape[0]):
+        if pg not in used:
+            Kp2[pg] = np.nan
+            Vp2[pg] = np.nan
+    table2 = table.copy()
+    table2[0, 2:] = -7          # invalid entries past the live pages are never looked at
+    table2[1, 3:] = 10**6
+    assert np.array_equal(oracle.decode_paged_f64(Q, Kp2, Vp2, table2, cp), base)
+
+
+def test_paged_invalid_live_page_gives_nan_row_only_for_that_sequence():
+    rng = np.random.default_rng(46)
+    B, H, D, ps, maxp = 3, 2, 8, 4, 3
+    Kp, Vp, table = _paged_case(rng, B, H, D, ps, maxp)
+    Q = rand_f16(rng, (B, H, D))
+    cp = np.array([11, 11, 11], np.uint32)
+    good = oracle.decode_paged_f64(Q, Kp, Vp, table, cp)
+    table[1, 1] = Kp.shape[0]  # out of range
+    got = oracle.decode_paged_f64(Q, Kp, Vp, table, cp)
+    assert np.isnan(got[1]).all()
+    assert np.array_equal(got[[0, 2]], good[[0, 2]])
