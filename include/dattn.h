@@ -54,7 +54,8 @@ enum dattn_status {
     DATTN_ERR_MISALIGNED = -3,  /* a tensor pointer is not 16-byte aligned          */
     DATTN_ERR_WORKSPACE = -4,   /* workspace missing, misaligned or too small       */
     DATTN_ERR_CUDA = -5,        /* a CUDA runtime call or kernel launch failed      */
-    DATTN_ERR_TIMEOUT = -6      /* a kernel gave up waiting on its own pipeline     */
+    DATTN_ERR_TIMEOUT = -6,     /* a kernel gave up waiting on its own pipeline     */
+    DATTN_ERR_BAD_PAGE = -7     /* a live position's block-table entry was invalid  */
 };
 
 /* Library version: major*10000 + minor*100 + patch. */
@@ -153,6 +154,32 @@ int dattn_decode_f16(const void *Q, const void *K_cache, const void *V_cache, vo
                      const uint32_t *current_pos, dattn_stream_t stream);
 
 /*
+ * Fused decode attention over a paged KV cache (the "direct page reads" form of
+ * decode attention in "Tutorial 16: Writing Custom Metal Kernels", section 7,
+ * for a cache held in fixed-size pages as the page-1 engine's paged block
+ * allocator does).  Same operation, output and rounding as dattn_decode_f16_ex;
+ * only the addressing of K and V differs:
+ *
+ *   K_pages, V_pages  [num_pages, page_size, n_heads, head_dim]   f16, device
+ *   block_table       [batch, max_pages]                          int32, device
+ *   K[b, p, h, :] = K_pages[block_table[b, p / page_size], p % page_size, h, :]
+ *
+ * Each sequence's capacity is seq_len = page_size * max_pages (< 2^31).
+ * Pages may be shared between sequences.  Entries for pages past a sequence's
+ * live length are never read.  A live entry outside [0, num_pages) is not
+ * dereferenced: page 0 is read instead, the output of that call is wrong, and
+ * dattn_device_error() reports DATTN_ERR_BAD_PAGE.  The workspace is the one of
+ * dattn_decode_workspace_bytes(batch, n_heads, head_dim, page_size * max_pages,
+ * num_partitions).
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA.
+ */
+int dattn_decode_paged_f16(const void *Q, const void *K_pages, const void *V_pages, void *out,
+                           int batch, int n_heads, int head_dim, int page_size, int max_pages,
+                           long long num_pages, const int32_t *block_table,
+                           const uint32_t *current_pos, void *workspace, size_t workspace_bytes,
+                           int num_partitions, dattn_stream_t stream);
+
+/*
  * The page's first dispatch, attention_qk_f16, batched ("The MSL, briefly"):
  *   scores[b,h,p] = half( (fp32 sum over i in index order of Q[b,h,i]*K[b,p,h,i],
  *                          each product and each sum rounded to fp32)
@@ -212,10 +239,12 @@ int dattn_decode_f16_noalloc(const void *Q, const void *K_cache, const void *V_c
  * Device-side error word of the current device.  Every wait inside the fused
  * kernel's shared-memory pipeline is bounded (about one second); a wait that
  * runs out records a code here, abandons its CTA's output and returns instead
- * of hanging the GPU.  This call synchronises the device, returns DATTN_OK if
- * no kernel has recorded an error since the last clear and DATTN_ERR_TIMEOUT
- * otherwise, and resets the word when `clear` is non-zero.
- * Errors: TIMEOUT, CUDA.
+ * of hanging the GPU.  The paged decode records invalid block-table entries
+ * here too.  This call synchronises the device and returns DATTN_OK if no
+ * kernel has recorded anything since the last clear, DATTN_ERR_TIMEOUT if a
+ * wait ran out, DATTN_ERR_BAD_PAGE if only a block-table entry was invalid;
+ * it resets the word when `clear` is non-zero.
+ * Errors: TIMEOUT, BAD_PAGE, CUDA.
  */
 int dattn_device_error(int clear);
 

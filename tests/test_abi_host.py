@@ -43,7 +43,8 @@ def test_version_and_status_strings(lib):
     assert lib.dattn_version() >= 10000
     for code, name in [(0, "DATTN_OK"), (-1, "DATTN_ERR_INVALID_ARG"), (-2, "DATTN_ERR_UNSUPPORTED"),
                        (-3, "DATTN_ERR_MISALIGNED"), (-4, "DATTN_ERR_WORKSPACE"),
-                       (-5, "DATTN_ERR_CUDA"), (-6, "DATTN_ERR_TIMEOUT")]:
+                       (-5, "DATTN_ERR_CUDA"), (-6, "DATTN_ERR_TIMEOUT"),
+                       (-7, "DATTN_ERR_BAD_PAGE")]:
         assert lib.dattn_status_string(code).decode() == name
 
 
@@ -85,6 +86,20 @@ def test_split_calls_reject_bad_arguments_on_host(lib):
     assert lib.dattn_pv_f16(A, None, A, 1, 2, 64, 16, None) == _native.ERR_INVALID_ARG
     assert lib.dattn_pv_f16(A, A, A, 1, 0, 64, 16, None) == _native.ERR_INVALID_ARG
     assert lib.dattn_decode_f16(A, A, A, None, 1, 2, 64, 16, A, None) == _native.ERR_INVALID_ARG
+
+
+def test_paged_decode_rejects_bad_arguments_on_host(lib):
+    def call(Q=A, K=A, V=A, out=A, B=1, H=2, D=64, ps=16, maxp=4, npages=8, table=A, cp=A):
+        return lib.dattn_decode_paged_f16(Q, K, V, out, B, H, D, ps, maxp, npages, table, cp,
+                                          A, 1 << 20, 0, None)
+    assert call(table=None) == _native.ERR_INVALID_ARG
+    assert call(table=A + 2) == _native.ERR_MISALIGNED
+    assert call(K=A + 8) == _native.ERR_MISALIGNED
+    assert call(ps=0) == _native.ERR_INVALID_ARG
+    assert call(maxp=-1) == _native.ERR_INVALID_ARG
+    assert call(npages=0) == _native.ERR_INVALID_ARG
+    assert call(ps=1 << 20, maxp=1 << 12) == _native.ERR_UNSUPPORTED
+    assert call(D=20) == _native.ERR_UNSUPPORTED
 
 
 def test_plan_queries_reject_bad_arguments_on_host(lib):

@@ -9,6 +9,7 @@ from ._native import (  # noqa: F401
     DattnError,
     dattn_decode_f16,
     dattn_decode_f16_ex,
+    dattn_decode_paged_f16,
     dattn_decode_plan,
     dattn_decode_workspace_bytes,
     dattn_device_error,
@@ -16,6 +17,7 @@ from ._native import (  # noqa: F401
     dattn_qk_f16,
     dattn_version,
     decode,
+    decode_paged,
     load,
     pv,
     qk,

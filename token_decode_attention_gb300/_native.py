@@ -38,8 +38,8 @@ class Plan(ctypes.Structure):
 
 
 # status codes (enum dattn_status)
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = (
-    0, -1, -2, -3, -4, -5, -6)
+(OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT,
+ ERR_BAD_PAGE) = (0, -1, -2, -3, -4, -5, -6, -7)
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -52,6 +52,8 @@ _SIGNATURES = {
     "dattn_decode_f16_ex": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, ctypes.c_size_t, _I, _P],
                             _I),
     "dattn_decode_f16": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P], _I),
+    "dattn_decode_paged_f16": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_longlong, _P, _P, _P,
+                                ctypes.c_size_t, _I, _P], _I),
     "dattn_decode_f16_noalloc": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P], _I),
     "dattn_qk_f16": ([_P, _P, _P, _I, _I, _I, _I, _P, _P], _I),
     "dattn_pv_f16": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
@@ -164,6 +166,28 @@ def dattn_decode_f16_ex(q, k, v, out, current_pos, workspace=None, num_partition
            "dattn_decode_f16_ex")
 
 
+def dattn_decode_paged_f16(q, k_pages, v_pages, out, block_table, current_pos, workspace=None,
+                           num_partitions: int = 0, stream=None) -> None:
+    if q.dim() != 3 or k_pages.dim() != 4 or block_table.dim() != 2:
+        raise ValueError("Q must be [batch, n_heads, head_dim], pages [num_pages, page_size, "
+                         "n_heads, head_dim], block_table [batch, max_pages]")
+    B, H, D = (int(x) for x in q.shape)
+    num_pages, page_size = int(k_pages.shape[0]), int(k_pages.shape[1])
+    max_pages = int(block_table.shape[1])
+    args = (_tensor(q, "Q", (B, H, D)), _tensor(k_pages, "K_pages", (num_pages, page_size, H, D)),
+            _tensor(v_pages, "V_pages", (num_pages, page_size, H, D)),
+            _tensor(out, "out", (B, H, D)))
+    table = _tensor(block_table, "block_table", (B, max_pages), torch.int32)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr = _tensor(workspace, "workspace", None, workspace.dtype)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().dattn_decode_paged_f16(*args, B, H, D, page_size, max_pages, num_pages, table,
+                                         _cur_pos(current_pos, B), ws_ptr, ws_bytes,
+                                         num_partitions, _stream_handle(stream)),
+           "dattn_decode_paged_f16")
+
+
 def dattn_decode_f16(q, k, v, out, current_pos, stream=None) -> None:
     B, H, D, S = _qkv_dims(q, k)
     _check(load().dattn_decode_f16(_tensor(q, "Q", (B, H, D)), _tensor(k, "K_cache", (B, S, H, D)),
@@ -197,7 +221,7 @@ def dattn_device_error(clear: bool = True) -> int:
     """Status of the device error word (DATTN_OK or DATTN_ERR_TIMEOUT); never raises on
     TIMEOUT, so callers can assert on it."""
     st = int(load().dattn_device_error(1 if clear else 0))
-    if st not in (OK, ERR_TIMEOUT):
+    if st not in (OK, ERR_TIMEOUT, ERR_BAD_PAGE):
         _check(st, "dattn_device_error")
     return st
 
@@ -218,6 +242,21 @@ def decode(q, k, v, current_pos, num_partitions: int = 0, out=None, workspace=No
         n = dattn_decode_workspace_bytes(B, H, D, S, num_partitions)
         workspace = torch.empty((max(n, 16),), dtype=torch.uint8, device=q.device)
     dattn_decode_f16_ex(q, k, v, out, current_pos, workspace, num_partitions, stream)
+    return out
+
+
+def decode_paged(q, k_pages, v_pages, block_table, current_pos, num_partitions: int = 0,
+                 out=None, workspace=None, stream=None):
+    """Fused decode over a paged cache; allocates ``out`` and the workspace if not given."""
+    B, H, D = (int(x) for x in q.shape)
+    S = int(k_pages.shape[1]) * int(block_table.shape[1])
+    if out is None:
+        out = torch.empty((B, H, D), dtype=torch.float16, device=q.device)
+    if workspace is None:
+        n = dattn_decode_workspace_bytes(B, H, D, S, num_partitions)
+        workspace = torch.empty((max(n, 16),), dtype=torch.uint8, device=q.device)
+    dattn_decode_paged_f16(q, k_pages, v_pages, out, block_table, current_pos, workspace,
+                           num_partitions, stream)
     return out
 
 

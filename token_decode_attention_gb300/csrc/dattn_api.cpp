@@ -288,9 +288,15 @@ int check_cur_pos(const uint32_t *cp) {
     return DATTN_OK;
 }
 
+struct Paging {
+    const int *table = nullptr;  // nullptr: dense [B, S, H, D] cache
+    long long num_pages = 0;
+    int page_size = 0, max_pages = 0;
+};
+
 int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, void *out, int B,
                   int H, int D, int S, const uint32_t *cur_pos, void *workspace,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, const Paging &pg = Paging()) {
     DeviceInfo di;
     if (int st = device_info(&di)) return st;
     char *ws = static_cast<char *>(workspace);
@@ -304,6 +310,10 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
     a.ws_acc = p.G > 1 ? reinterpret_cast<float *>(ws + p.prefix_bytes) : nullptr;
     a.ws_ml = p.G > 1 ? reinterpret_cast<float2 *>(ws + p.prefix_bytes + p.acc_bytes) : nullptr;
     a.err = di.err_word;
+    a.block_table = pg.table;
+    a.num_pages = pg.num_pages;
+    a.page_size = pg.page_size;
+    a.max_pages = pg.max_pages;
     a.B = B;
     a.H = H;
     a.D = D;
@@ -370,6 +380,7 @@ const char *dattn_status_string(int status) {
         case DATTN_ERR_WORKSPACE: return "DATTN_ERR_WORKSPACE";
         case DATTN_ERR_CUDA: return "DATTN_ERR_CUDA";
         case DATTN_ERR_TIMEOUT: return "DATTN_ERR_TIMEOUT";
+        case DATTN_ERR_BAD_PAGE: return "DATTN_ERR_BAD_PAGE";
         default: return "DATTN_ERR_UNKNOWN";
     }
 }
@@ -463,6 +474,53 @@ int dattn_decode_f16(const void *Q, const void *K_cache, const void *V_cache, vo
                          current_pos, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int dattn_decode_paged_f16(const void *Q, const void *K_pages, const void *V_pages, void *out,
+                           int batch, int n_heads, int head_dim, int page_size, int max_pages,
+                           long long num_pages, const int32_t *block_table,
+                           const uint32_t *current_pos, void *workspace, size_t workspace_bytes,
+                           int num_partitions, dattn_stream_t stream) {
+    if (int st = check_tensor(Q, "Q")) return st;
+    if (int st = check_tensor(K_pages, "K_pages")) return st;
+    if (int st = check_tensor(V_pages, "V_pages")) return st;
+    if (int st = check_tensor(out, "out")) return st;
+    if (int st = check_cur_pos(current_pos)) return st;
+    if (block_table == nullptr) return fail(DATTN_ERR_INVALID_ARG, "block_table is NULL");
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0)
+        return fail(DATTN_ERR_MISALIGNED, "block_table is not 4-byte aligned");
+    if (page_size <= 0 || max_pages <= 0 || num_pages <= 0)
+        return fail(DATTN_ERR_INVALID_ARG,
+                    "page_size=%d, max_pages=%d and num_pages=%lld must be positive", page_size,
+                    max_pages, num_pages);
+    const long long cap = static_cast<long long>(page_size) * max_pages;
+    if (cap > 0x7fffffffLL)
+        return fail(DATTN_ERR_UNSUPPORTED, "page_size x max_pages = %lld exceeds 2^31 - 1", cap);
+    if (static_cast<double>(num_pages) * page_size * n_heads * head_dim > 4.0e18)
+        return fail(DATTN_ERR_INVALID_ARG, "page pool is too large");
+    const int S = static_cast<int>(cap);
+    if (int st = validate_dims(batch, n_heads, head_dim, S)) return st;
+    if (num_partitions < 0)
+        return fail(DATTN_ERR_INVALID_ARG, "num_partitions=%d must be >= 0", num_partitions);
+    Plan p;
+    if (int st = make_plan(batch, n_heads, head_dim, S, num_partitions, &p)) return st;
+    if (p.ws_bytes > 0) {
+        if (workspace == nullptr)
+            return fail(DATTN_ERR_WORKSPACE, "workspace of %zu bytes required, got NULL",
+                        p.ws_bytes);
+        if (!aligned16(workspace))
+            return fail(DATTN_ERR_WORKSPACE, "workspace is not 16-byte aligned");
+        if (workspace_bytes < p.ws_bytes)
+            return fail(DATTN_ERR_WORKSPACE, "workspace of %zu bytes required, got %zu",
+                        p.ws_bytes, workspace_bytes);
+    }
+    Paging pg;
+    pg.table = block_table;
+    pg.num_pages = num_pages;
+    pg.page_size = page_size;
+    pg.max_pages = max_pages;
+    return launch_decode(p, Q, K_pages, V_pages, out, batch, n_heads, head_dim, S, current_pos,
+                         workspace, reinterpret_cast<cudaStream_t>(stream), pg);
+}
+
 int dattn_qk_f16(const void *Q, const void *K_cache, void *scores, int batch, int n_heads,
                  int head_dim, int seq_len, const uint32_t *current_pos,
                  dattn_stream_t stream) {
@@ -508,8 +566,11 @@ int dattn_device_error(int clear) {
         if (e == cudaSuccess) e = cudaDeviceSynchronize();
         if (e != cudaSuccess) return fail_cuda(e, "cudaMemset (error word)");
     }
-    if (word != 0)
+    if (word & ~dattn::kErrPageIndex)
         return fail(DATTN_ERR_TIMEOUT, "a kernel gave up on a pipeline wait (code 0x%x)", word);
+    if (word & dattn::kErrPageIndex)
+        return fail(DATTN_ERR_BAD_PAGE,
+                    "a block-table entry of a live position was outside [0, num_pages)");
     return DATTN_OK;
 }
 

@@ -19,6 +19,7 @@ constexpr unsigned kErrConsumerWait = 1u;
 constexpr unsigned kErrProducerWait = 2u;
 constexpr unsigned kErrDrainWait = 4u;
 constexpr unsigned kErrSelftestWait = 8u;
+constexpr unsigned kErrPageIndex = 16u;  // a block-table entry outside [0, num_pages)
 
 // Time limit of every pipeline wait in the library's kernels.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // one second
@@ -41,6 +42,13 @@ struct DecodeArgs {
     float *ws_acc;            // [(G+U), HG, D] unnormalised partial outputs
     float2 *ws_ml;            // [(G+U), HG]    partial (running max, log2 units; sum)
     unsigned *err;            // device error word
+    // Paged cache (block_table != nullptr): K and V are pages
+    // [num_pages, page_size, H, D] and position p of sequence b lives in page
+    // block_table[b * max_pages + p / page_size], row p % page_size.  S is then
+    // page_size * max_pages.
+    const int *block_table;
+    long long num_pages;
+    int page_size, max_pages;
     int B, H, D, S;
     int heads_per_cta;  // HG
     int head_groups;    // NHG

@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         // ---------------- producer warp ----------------
         const uint64_t policy = l2_evict_first_policy();
         const size_t pos_stride = static_cast<size_t>(a.H) * D;  // halves between positions
+        const bool paged = a.block_table != nullptr;
         int st = 0, issued = 0;
         bool go = true;
         while (go && next_piece(walk, a)) {
@@ -256,6 +257,9 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
             const __half *Vb = reinterpret_cast<const __half *>(a.V) + seq_base;
             const uint32_t row_bytes = static_cast<uint32_t>(hg) * D * 2;
             const bool contiguous = (hg == a.H);
+            // paged cache: lane i holds block_table[b][page_first + i]
+            const int *bt = paged ? a.block_table + walk.b * a.max_pages : nullptr;
+            int page_first = -1, page_lane = 0;
             for (int p = 0; p < walk.len; p += a.stage_pos, ++st) {
                 const int slot = st % a.stages;
                 int ok = 1;
@@ -274,24 +278,63 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                     break;
                 }
                 const int np = min(a.stage_pos, walk.len - p);
-                const size_t pos0 = static_cast<size_t>(walk.off + p);
+                const int pos0 = walk.off + p;
                 __half *dK = ring + static_cast<size_t>(slot) * 2 * buf_elems;
                 __half *dV = dK + buf_elems;
-                const __half *sK = Kb + pos0 * pos_stride;
-                const __half *sV = Vb + pos0 * pos_stride;
                 if (lane == 0) mbar_arrive_expect_tx(&full_bar[slot], 2u * np * row_bytes);
                 __syncwarp();
-                if (contiguous) {
-                    if (lane == 0) {
-                        bulk_g2s(dK, sK, np * row_bytes, &full_bar[slot], policy);
-                        bulk_g2s(dV, sV, np * row_bytes, &full_bar[slot], policy);
+                if (!paged) {
+                    const __half *sK = Kb + static_cast<size_t>(pos0) * pos_stride;
+                    const __half *sV = Vb + static_cast<size_t>(pos0) * pos_stride;
+                    if (contiguous) {
+                        if (lane == 0) {
+                            bulk_g2s(dK, sK, np * row_bytes, &full_bar[slot], policy);
+                            bulk_g2s(dV, sV, np * row_bytes, &full_bar[slot], policy);
+                        }
+                    } else {
+                        for (int j = lane; j < np; j += 32) {
+                            bulk_g2s(dK + static_cast<size_t>(j) * hg * D, sK + j * pos_stride,
+                                     row_bytes, &full_bar[slot], policy);
+                            bulk_g2s(dV + static_cast<size_t>(j) * hg * D, sV + j * pos_stride,
+                                     row_bytes, &full_bar[slot], policy);
+                        }
                     }
                 } else {
-                    for (int j = lane; j < np; j += 32) {
-                        bulk_g2s(dK + static_cast<size_t>(j) * hg * D, sK + j * pos_stride,
-                                 row_bytes, &full_bar[slot], policy);
-                        bulk_g2s(dV + static_cast<size_t>(j) * hg * D, sV + j * pos_stride,
-                                 row_bytes, &full_bar[slot], policy);
+                    // split the stage into runs that stay inside one page
+                    for (int j = 0; j < np;) {
+                        const int pos = pos0 + j;
+                        const int pidx = pos / a.page_size;
+                        const int off = pos - pidx * a.page_size;
+                        if (page_first < 0 || pidx < page_first || pidx >= page_first + 32) {
+                            page_first = pidx;
+                            page_lane = (pidx + lane < a.max_pages) ? __ldg(bt + pidx + lane) : 0;
+                        }
+                        long long page = __shfl_sync(kFull, page_lane, pidx - page_first);
+                        if (page < 0 || page >= a.num_pages) {  // never read outside the pages
+                            if (lane == 0) atomicOr(a.err, kErrPageIndex);
+                            page = 0;
+                        }
+                        const int run = min(a.page_size - off, np - j);
+                        const size_t src = (static_cast<size_t>(page) * a.page_size + off) * pos_stride +
+                                           static_cast<size_t>(h0) * D;
+                        const __half *sK = reinterpret_cast<const __half *>(a.K) + src;
+                        const __half *sV = reinterpret_cast<const __half *>(a.V) + src;
+                        __half *tK = dK + static_cast<size_t>(j) * hg * D;
+                        __half *tV = dV + static_cast<size_t>(j) * hg * D;
+                        if (contiguous) {
+                            if (lane == 0) {
+                                bulk_g2s(tK, sK, run * row_bytes, &full_bar[slot], policy);
+                                bulk_g2s(tV, sV, run * row_bytes, &full_bar[slot], policy);
+                            }
+                        } else {
+                            for (int r = lane; r < run; r += 32) {
+                                bulk_g2s(tK + static_cast<size_t>(r) * hg * D, sK + r * pos_stride,
+                                         row_bytes, &full_bar[slot], policy);
+                                bulk_g2s(tV + static_cast<size_t>(r) * hg * D, sV + r * pos_stride,
+                                         row_bytes, &full_bar[slot], policy);
+                            }
+                        }
+                        j += run;
                     }
                 }
                 ++issued;
