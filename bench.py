@@ -182,11 +182,29 @@ def all_ranks_sum(x: int, world: int, device) -> int:
 
 # ------------------------------------------------------------- our arm
 
+def to_pages(x: dict, page_size: int, seed: int) -> dict:
+    """The same cache held in pages of `page_size` positions, in a seeded random
+    order of the page pool, with the block table that maps it back."""
+    B, S, H, D = x["k"].shape
+    if S % page_size:
+        raise ValueError(f"seq_len {S} is not a multiple of page_size {page_size}")
+    maxp = S // page_size
+    perm = torch.from_numpy(np.random.default_rng(seed).permutation(B * maxp)).to(x["k"].device)
+    out = {"q": x["q"], "cur_pos": x["cur_pos"],
+           "table": perm.view(B, maxp).to(torch.int32).contiguous()}
+    for key in ("k", "v"):
+        pages = torch.empty((B * maxp, page_size, H, D), dtype=x[key].dtype, device=x[key].device)
+        pages[perm] = x[key].view(B * maxp, page_size, H, D)
+        out[key] = pages
+        x[key] = None  # the dense copy is no longer needed
+    return out
+
+
 class Replica:
     """Input sets, outputs and workspace of one workload on one GPU."""
 
     def __init__(self, name: str, device, l2_bytes: int, partitions: int = 0,
-                 batch: int = 0):
+                 batch: int = 0, page_size: int = 0):
         import dataclasses
 
         import token_decode_attention_gb300 as dattn
@@ -201,10 +219,13 @@ class Replica:
         self.sets_n = 1 if kv >= 4 * l2_bytes else min(4096, math.ceil(4 * l2_bytes / kv) + 1)
         base = make_inputs(WORKLOADS[name], device, batch=w.batch)
         self.cp_host = base["cur_pos_host"]
+        self.page_size = page_size
+        if page_size:
+            base = to_pages(base, page_size, w.seed)
         self.sets = [base]
         for i in range(1, self.sets_n):
-            self.sets.append({"q": base["q"].clone(), "k": base["k"].clone(),
-                              "v": base["v"].clone(), "cur_pos": base["cur_pos"]})
+            self.sets.append({key: (val.clone() if key in ("q", "k", "v") else val)
+                              for key, val in base.items()})
         self.outs = [torch.empty((w.batch, w.n_heads, w.head_dim), dtype=torch.float16,
                                  device=device) for _ in range(self.sets_n)]
         self.partitions = partitions
@@ -221,8 +242,13 @@ class Replica:
 
     def step(self, i: int, stream):
         x = self.sets[i % self.sets_n]
-        self.dattn.dattn_decode_f16_ex(x["q"], x["k"], x["v"], self.outs[i % self.sets_n],
-                                       x["cur_pos"], self.ws, self.partitions, stream)
+        if self.page_size:
+            self.dattn.dattn_decode_paged_f16(x["q"], x["k"], x["v"], self.outs[i % self.sets_n],
+                                              x["table"], x["cur_pos"], self.ws, self.partitions,
+                                              stream)
+        else:
+            self.dattn.dattn_decode_f16_ex(x["q"], x["k"], x["v"], self.outs[i % self.sets_n],
+                                           x["cur_pos"], self.ws, self.partitions, stream)
 
     def timed(self, steps: int, warmup: int, stream, world: int, soak_s: float = 1.0,
               sampler: ClockSampler | None = None, graph: bool = True):
@@ -279,6 +305,8 @@ class Replica:
         Q, the new token's K/V row and current_pos from pinned host memory,
         appends the K/V row at current_pos, runs the decode and reads out back
         into pinned host memory.  The KV cache itself is device-resident state."""
+        if self.page_size:
+            return None  # measured on the dense layout only
         w = self.w
         x = self.sets[0]
         B, H, D = w.batch, w.n_heads, w.head_dim
@@ -357,20 +385,23 @@ def cpu_baseline(name: str, budget_s: float, max_reps: int = 1000) -> dict:
 
 def sweep(device, stream, l2_bytes: int, steps: int, warmup: int, peak: float) -> dict:
     res = {}
-    for name in ("small", "7b", "ragged", "long", "outlier"):
+    runs = [(n, 0) for n in ("small", "7b", "ragged", "long", "outlier")]
+    runs += [(n, 16) for n in ("7b", "ragged", "long", "outlier")]
+    for name, ps in runs:
+        key = name if not ps else f"{name}_paged{ps}"
         try:
-            r = Replica(name, device, l2_bytes)
+            r = Replica(name, device, l2_bytes, page_size=ps)
             ms, _ = r.timed(steps, warmup, stream, 1, soak_s=0.2)
             t = ms * 1e-3 / steps
             gbs = r.bytes_per_step / t / 1e9
-            res[name] = {"us_per_step": t * 1e6, "GB/s": gbs, "frac_of_measured": gbs / peak,
+            res[key] = {"us_per_step": t * 1e6, "GB/s": gbs, "frac_of_measured": gbs / peak,
                          "frac_of_nominal_8TBs": gbs / NOMINAL_HBM_GBS,
                          "query_heads_per_s": r.w.batch * r.w.n_heads / t,
                          "partitions": r.plan["partitions"],
                          "algorithmic_bytes": r.bytes_per_step, "l2": r.l2_note}
             del r
         except Exception as e:  # report, keep going
-            res[name] = {"error": f"{type(e).__name__}: {e}"}
+            res[key] = {"error": f"{type(e).__name__}: {e}"}
         torch.cuda.empty_cache()
     return res
 
@@ -422,6 +453,8 @@ def main():
                     help="issue the timed steps from Python instead of a CUDA graph")
     ap.add_argument("--partitions", type=int, default=0,
                     help="force the number of decode partitions (0 = library choice)")
+    ap.add_argument("--paged", type=int, default=0,
+                    help="hold the cache in pages of this many positions (0 = dense)")
     ap.add_argument("--batch", type=int, default=0,
                     help="with --profile: fewer sequences of the same recipe")
     ap.add_argument("--profile", action="store_true",
@@ -454,7 +487,7 @@ def main():
     stream = torch.cuda.Stream(device=device)
 
     rep = Replica(args.workload, device, l2, args.partitions,
-                  args.batch if args.profile else 0)
+                  args.batch if args.profile else 0, args.paged)
     sampler = ClockSampler(local)
     if args.profile:
         ms, _ = rep.timed(args.steps, args.warmup, stream, world, soak_s=0.0,
