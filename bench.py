@@ -236,6 +236,10 @@ class Replica:
         self.bytes_per_step = algorithmic_bytes(w.batch, w.n_heads, w.head_dim, w.seq_len,
                                                 self.cp_host)
         self.launches_per_step = 1 + (1 if self.plan["partitions"] > 1 else 0)
+        # Everything above ran on the default stream; the steps run on a side
+        # stream.  Finish it here so no buffer freed by the set-up (and reused
+        # by the allocator) is still being read when the side stream writes.
+        torch.cuda.synchronize(device)
         self.l2_note = (f"inputs larger than L2 ({kv / 2**30:.2f} GiB K+V)" if self.sets_n == 1
                         else f"rotating {self.sets_n} input sets, {self.sets_n * kv / 2**30:.2f}"
                              f" GiB K+V in total (> 4x L2)")
@@ -259,6 +263,7 @@ class Replica:
         once: the GPU runs the K decode calls back to back, as a decode loop
         under graph submission does.  With graph=False the calls are issued
         eagerly from Python, so host overhead per call is included."""
+        stream.wait_stream(torch.cuda.current_stream(self.device))
         with torch.cuda.stream(stream):
             for i in range(warmup):
                 self.step(i, stream)
@@ -326,6 +331,8 @@ class Replica:
         out_d = self.outs[0]
         h2d = (q_h.numel() + knew_h.numel() + vnew_h.numel()) * 2 + cp_h.numel() * 4
         d2h = out_h.numel() * 2
+
+        stream.wait_stream(torch.cuda.current_stream(self.device))
 
         def one():
             q_d.copy_(q_h, non_blocking=True)
@@ -401,6 +408,8 @@ def sweep(device, stream, l2_bytes: int, steps: int, warmup: int, peak: float) -
                          "algorithmic_bytes": r.bytes_per_step, "l2": r.l2_note}
             del r
         except Exception as e:  # report, keep going
+            import traceback
+            traceback.print_exc(file=sys.stderr)
             res[key] = {"error": f"{type(e).__name__}: {e}"}
         torch.cuda.empty_cache()
     return res
