@@ -236,6 +236,34 @@ int dattn_decode_f16_noalloc(const void *Q, const void *K_cache, const void *V_c
                              const uint32_t *current_pos, dattn_stream_t stream);
 
 /*
+ * Submission batching: the analogue of the fm_batch_begin / fm_batch_end pair
+ * of the C API in Foundry's docs/metal.md (section "Command Batching"), which
+ * accumulates operations into one GPU submission.  Here the calls issued on a
+ * stream between dattn_batch_begin and dattn_batch_end are recorded (CUDA
+ * stream capture, thread-local mode) instead of run; dattn_batch_end turns
+ * them into a replayable batch and dattn_batch_launch submits all of them at
+ * once on any stream, as often as wanted.  A replay reads the buffers the
+ * recorded calls were given, with their contents at replay time: to decode a
+ * new token, write the new Q / cache rows / current_pos into the same buffers
+ * and launch again.
+ *
+ * Calls that may be recorded: dattn_decode_f16_ex, dattn_decode_paged_f16,
+ * dattn_decode_f16_noalloc after its first call on the device, dattn_qk_f16,
+ * dattn_pv_f16, and dattn_decode_f16 once its workspace is large enough (a
+ * recorded call must not allocate).  The shape's plan is made when a call is
+ * recorded; make one ordinary call per shape first if its set-up should not
+ * happen during recording.  `stream` must be a created stream, not NULL.
+ * Errors: INVALID_ARG, CUDA (for example a recorded call that synchronised).
+ */
+typedef struct dattn_batch dattn_batch;
+int dattn_batch_begin(dattn_stream_t stream);
+int dattn_batch_end(dattn_stream_t stream, dattn_batch **batch);
+int dattn_batch_launch(const dattn_batch *batch, dattn_stream_t stream);
+/* Number of GPU operations recorded in a batch (-1 for NULL). */
+long long dattn_batch_nodes(const dattn_batch *batch);
+int dattn_batch_destroy(dattn_batch *batch);
+
+/*
  * Device-side error word of the current device.  Every wait inside the fused
  * kernel's shared-memory pipeline is bounded (about one second); a wait that
  * runs out records a code here, abandons its CTA's output and returns instead

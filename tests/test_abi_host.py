@@ -119,3 +119,12 @@ def test_python_binding_rejects_cpu_tensors():
         _native.dattn_decode_f16_ex(q, k, k, q, cp)
     with pytest.raises(TypeError):
         _native.dattn_decode_f16_ex(q.float(), k, k, q, cp)
+
+
+def test_batch_api_rejects_bad_arguments_on_host(lib):
+    import ctypes as C
+    assert lib.dattn_batch_begin(None) == _native.ERR_INVALID_ARG  # the legacy stream
+    assert lib.dattn_batch_end(A, None) == _native.ERR_INVALID_ARG
+    assert lib.dattn_batch_launch(None, None) == _native.ERR_INVALID_ARG
+    assert lib.dattn_batch_nodes(None) == -1
+    assert lib.dattn_batch_destroy(None) == _native.OK

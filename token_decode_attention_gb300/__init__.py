@@ -6,7 +6,10 @@ its ctypes binding and the seeded synthetic workloads; the binding is loaded on
 first use and raises if the library has not been built.
 """
 from ._native import (  # noqa: F401
+    Batch,
     DattnError,
+    dattn_batch_begin,
+    dattn_batch_end,
     dattn_decode_f16,
     dattn_decode_f16_ex,
     dattn_decode_paged_f16,

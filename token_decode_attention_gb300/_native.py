@@ -59,6 +59,11 @@ _SIGNATURES = {
     "dattn_pv_f16": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
     "dattn_device_error": ([_I], _I),
     "dattn_selftest_wait_timeout": ([_P], _I),
+    "dattn_batch_begin": ([_P], _I),
+    "dattn_batch_end": ([_P, ctypes.POINTER(ctypes.c_void_p)], _I),
+    "dattn_batch_launch": ([_P, _P], _I),
+    "dattn_batch_nodes": ([_P], ctypes.c_longlong),
+    "dattn_batch_destroy": ([_P], _I),
 }
 
 
@@ -229,6 +234,43 @@ def dattn_device_error(clear: bool = True) -> int:
 def dattn_selftest_wait_timeout(stream=None) -> None:
     _check(load().dattn_selftest_wait_timeout(_stream_handle(stream)),
            "dattn_selftest_wait_timeout")
+
+
+class Batch:
+    """Calls recorded between dattn_batch_begin and dattn_batch_end on a stream,
+    replayed as one submission (see include/dattn.h)."""
+
+    def __init__(self, handle: int):
+        self.handle = handle
+
+    def launch(self, stream=None) -> None:
+        _check(load().dattn_batch_launch(self.handle, _stream_handle(stream)),
+               "dattn_batch_launch")
+
+    @property
+    def nodes(self) -> int:
+        return int(load().dattn_batch_nodes(self.handle))
+
+    def close(self) -> None:
+        if self.handle:
+            _check(load().dattn_batch_destroy(self.handle), "dattn_batch_destroy")
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def dattn_batch_begin(stream) -> None:
+    _check(load().dattn_batch_begin(_stream_handle(stream)), "dattn_batch_begin")
+
+
+def dattn_batch_end(stream) -> Batch:
+    h = ctypes.c_void_p(0)
+    _check(load().dattn_batch_end(_stream_handle(stream), ctypes.byref(h)), "dattn_batch_end")
+    return Batch(h.value)
 
 
 # ------------------------------------------------------- convenience forms

@@ -553,6 +553,57 @@ int dattn_selftest_wait_timeout(dattn_stream_t stream) {
     return e == cudaSuccess ? DATTN_OK : fail_cuda(e, "self-test kernel launch");
 }
 
+struct dattn_batch {
+    cudaGraphExec_t exec = nullptr;
+    size_t nodes = 0;
+};
+
+int dattn_batch_begin(dattn_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (s == nullptr)
+        return fail(DATTN_ERR_INVALID_ARG, "batches need a created stream, not the legacy default");
+    const cudaError_t e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+    return e == cudaSuccess ? DATTN_OK : fail_cuda(e, "cudaStreamBeginCapture");
+}
+
+int dattn_batch_end(dattn_stream_t stream, dattn_batch **batch) {
+    if (batch == nullptr) return fail(DATTN_ERR_INVALID_ARG, "batch is NULL");
+    *batch = nullptr;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(s, &graph);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamEndCapture");
+    dattn_batch *b = new dattn_batch();
+    e = cudaGraphGetNodes(graph, nullptr, &b->nodes);
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&b->exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) {
+        delete b;
+        return fail_cuda(e, "cudaGraphInstantiate");
+    }
+    *batch = b;
+    return DATTN_OK;
+}
+
+int dattn_batch_launch(const dattn_batch *batch, dattn_stream_t stream) {
+    if (batch == nullptr || batch->exec == nullptr)
+        return fail(DATTN_ERR_INVALID_ARG, "batch is NULL");
+    const cudaError_t e = cudaGraphLaunch(batch->exec, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DATTN_OK : fail_cuda(e, "cudaGraphLaunch");
+}
+
+long long dattn_batch_nodes(const dattn_batch *batch) {
+    return batch == nullptr ? -1 : static_cast<long long>(batch->nodes);
+}
+
+int dattn_batch_destroy(dattn_batch *batch) {
+    if (batch == nullptr) return DATTN_OK;
+    cudaError_t e = cudaSuccess;
+    if (batch->exec != nullptr) e = cudaGraphExecDestroy(batch->exec);
+    delete batch;
+    return e == cudaSuccess ? DATTN_OK : fail_cuda(e, "cudaGraphExecDestroy");
+}
+
 int dattn_device_error(int clear) {
     DeviceInfo di;
     if (int st = device_info(&di)) return st;
