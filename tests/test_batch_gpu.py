@@ -47,18 +47,21 @@ def test_recorded_decodes_replay_on_new_contents():
     out2 = torch.empty_like(q2)
     ws2 = torch.empty(max(16, dattn.dattn_decode_workspace_bytes(B2, H2, D2, ps * maxp)),
                       dtype=torch.uint8, device="cuda")
-    # call 3: the library-owned workspace, grown by one ordinary call first
-    out3 = torch.empty_like(q1)
-    dattn.dattn_decode_f16(q1, k1, v1, out3, cp1)
-    torch.cuda.synchronize()
-
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
-    dattn.dattn_batch_begin(s)
-    dattn.dattn_decode_f16_ex(q1, k1, v1, out1, cp1, ws1, 0, s)
-    dattn.dattn_decode_paged_f16(q2, kp, vp, out2, table, cp2, ws2, 0, s)
+    # call 3: the library-owned workspace of stream s, grown by one ordinary
+    # call on s before recording
+    out3 = torch.empty_like(q1)
     dattn.dattn_decode_f16(q1, k1, v1, out3, cp1, s)
-    batch = dattn.dattn_batch_end(s)
+    torch.cuda.synchronize()
+
+    dattn.dattn_batch_begin(s)
+    try:
+        dattn.dattn_decode_f16_ex(q1, k1, v1, out1, cp1, ws1, 0, s)
+        dattn.dattn_decode_paged_f16(q2, kp, vp, out2, table, cp2, ws2, 0, s)
+        dattn.dattn_decode_f16(q1, k1, v1, out3, cp1, s)
+    finally:
+        batch = dattn.dattn_batch_end(s)
     assert batch.nodes >= 3
     torch.cuda.synchronize()
 
@@ -78,3 +81,25 @@ def test_recorded_decodes_replay_on_new_contents():
         assert_decode_close(out2, ref2, f"replay {replay}, paged")
     batch.close()
     assert dattn.dattn_device_error(clear=True) == _native.OK
+
+
+def test_growing_the_library_workspace_while_recording_is_refused_cleanly():
+    g = torch.Generator(device="cuda").manual_seed(9)
+    B, H, D, S = 1, 32, 128, 5000
+    q, k, v = rand_f16(g, (B, H, D)), rand_f16(g, (B, S, H, D)), rand_f16(g, (B, S, H, D))
+    out = torch.empty_like(q)
+    s = torch.cuda.Stream()  # a fresh stream: its library workspace does not exist yet
+    s.wait_stream(torch.cuda.current_stream())
+    dattn.dattn_batch_begin(s)
+    try:
+        with pytest.raises(_native.DattnError) as ei:
+            dattn.dattn_decode_f16(q, k, v, out, cur_pos_tensor([4999]), s)
+        assert ei.value.status == _native.ERR_WORKSPACE
+    finally:
+        batch = dattn.dattn_batch_end(s)
+    batch.close()
+    # outside recording the same call works
+    dattn.dattn_decode_f16(q, k, v, out, cur_pos_tensor([4999]), s)
+    torch.cuda.synchronize()
+    ref = oracle.decode_f64(to_np(q), to_np(k), to_np(v), np.array([4999], np.uint32))
+    assert_decode_close(out, ref, "after the refused recording")

@@ -459,7 +459,16 @@ int dattn_decode_f16(const void *Q, const void *K_cache, const void *V_cache, vo
         std::lock_guard<std::mutex> lock(g_ws_mutex);
         OwnedWorkspace &w = g_workspaces[{dev, reinterpret_cast<cudaStream_t>(stream)}];
         if (w.bytes < p.ws_bytes) {
-            cudaError_t e = cudaDeviceSynchronize();
+            cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+            cudaError_t e = cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cap);
+            if (e != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
+            if (cap != cudaStreamCaptureStatusNone)
+                return fail(DATTN_ERR_WORKSPACE,
+                            "the library workspace of this stream must grow to %zu bytes, which "
+                            "cannot happen while the stream is being recorded; make one call on "
+                            "this stream before recording",
+                            p.ws_bytes);
+            e = cudaDeviceSynchronize();
             if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize (workspace grow)");
             if (w.ptr != nullptr) cudaFree(w.ptr);
             w.ptr = nullptr;
