@@ -88,18 +88,20 @@ def test_growing_the_library_workspace_while_recording_is_refused_cleanly():
     B, H, D, S = 1, 32, 128, 5000
     q, k, v = rand_f16(g, (B, H, D)), rand_f16(g, (B, S, H, D)), rand_f16(g, (B, S, H, D))
     out = torch.empty_like(q)
+    cp = cur_pos_tensor([4999])  # made before recording: no copies while recording
     s = torch.cuda.Stream()  # a fresh stream: its library workspace does not exist yet
     s.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
     dattn.dattn_batch_begin(s)
     try:
         with pytest.raises(_native.DattnError) as ei:
-            dattn.dattn_decode_f16(q, k, v, out, cur_pos_tensor([4999]), s)
+            dattn.dattn_decode_f16(q, k, v, out, cp, s)
         assert ei.value.status == _native.ERR_WORKSPACE
     finally:
         batch = dattn.dattn_batch_end(s)
     batch.close()
     # outside recording the same call works
-    dattn.dattn_decode_f16(q, k, v, out, cur_pos_tensor([4999]), s)
+    dattn.dattn_decode_f16(q, k, v, out, cp, s)
     torch.cuda.synchronize()
     ref = oracle.decode_f64(to_np(q), to_np(k), to_np(v), np.array([4999], np.uint32))
     assert_decode_close(out, ref, "after the refused recording")

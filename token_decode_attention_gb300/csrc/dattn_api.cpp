@@ -329,7 +329,6 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
     a.bar_offset = p.bar_offset;
     a.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     cudaError_t e = dattn::launch_decode(a, p.v, p.smem, stream);
-    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail_cuda(e, "decode kernel launch");
     if (p.G > 1) {
         dattn::CombineArgs c{};
@@ -347,7 +346,6 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
         c.partitions = p.G;
         c.chunk = p.combine_chunk;
         e = dattn::launch_combine(c, stream);
-        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return fail_cuda(e, "combine kernel launch");
     }
     return DATTN_OK;

@@ -28,8 +28,9 @@ __global__ void wait_timeout_selftest_kernel(unsigned *err) {
 }  // namespace
 
 cudaError_t launch_wait_timeout_selftest(unsigned *err, cudaStream_t stream) {
-    wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(err);
-    return cudaGetLastError();
+    void *args[] = {&err};
+    return cudaLaunchKernel(reinterpret_cast<const void *>(wait_timeout_selftest_kernel), dim3(1),
+                            dim3(32), args, 0, stream);
 }
 
 }  // namespace dattn

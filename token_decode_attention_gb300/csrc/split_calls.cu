@@ -121,20 +121,24 @@ cudaError_t launch_qk(const void *Q, const void *K, void *scores, int B, int H, 
     const long long total = static_cast<long long>(B) * H * S;
     const long long blocks = (total + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    qk_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const __half *>(Q), static_cast<const __half *>(K),
-        static_cast<__half *>(scores), B, H, D, S, cur_pos);
-    return cudaGetLastError();
+    const __half *q = static_cast<const __half *>(Q);
+    const __half *k = static_cast<const __half *>(K);
+    __half *sc = static_cast<__half *>(scores);
+    void *args[] = {&q, &k, &sc, &B, &H, &D, &S, const_cast<const uint32_t **>(&cur_pos)};
+    return cudaLaunchKernel(reinterpret_cast<const void *>(qk_kernel),
+                            dim3(static_cast<unsigned>(blocks)), dim3(256), args, 0, stream);
 }
 
 cudaError_t launch_pv(const void *scores, const void *V, void *out, int B, int H, int D, int S,
                       cudaStream_t stream) {
     const long long blocks = static_cast<long long>(B) * H;
     if (blocks > 0x7fffffffLL || D > kPvThreads) return cudaErrorInvalidValue;
-    pv_kernel<<<static_cast<unsigned>(blocks), kPvThreads, 0, stream>>>(
-        static_cast<const __half *>(scores), static_cast<const __half *>(V),
-        static_cast<__half *>(out), H, D, S);
-    return cudaGetLastError();
+    const __half *sc = static_cast<const __half *>(scores);
+    const __half *v = static_cast<const __half *>(V);
+    __half *o = static_cast<__half *>(out);
+    void *args[] = {&sc, &v, &o, &H, &D, &S};
+    return cudaLaunchKernel(reinterpret_cast<const void *>(pv_kernel),
+                            dim3(static_cast<unsigned>(blocks)), dim3(kPvThreads), args, 0, stream);
 }
 
 }  // namespace dattn
