@@ -43,7 +43,7 @@ def _worker(rank: int, world: int, port: int, results):
 
 def test_whole_job_takes_slowest_rank_and_sums_work():
     world, port = 2, _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.spawn(_worker, args=(world, port, results), nprocs=world, join=True)
         r0, r1 = results[0], results[1]
