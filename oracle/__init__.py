@@ -40,6 +40,8 @@ def _load(path: str):
     lib.oracle_f16_to_f64_array.argtypes = [u16p, f64p, i64]
     lib.oracle_f32_to_f16_array.argtypes = [ctypes.POINTER(ctypes.c_float), u16p, i64]
     lib.oracle_max_threads.restype = ctypes.c_int
+    lib.oracle_softmax_f64.argtypes = [ctypes.POINTER(ctypes.c_float), i64, i64, f64p,
+                                       ctypes.c_int]
     lib.oracle_decode_paged_f64.argtypes = [u16p, u16p, u16p, i64, i64, i64, i64, i64,
                                             ctypes.POINTER(ctypes.c_int32), i64, u32p, f64p,
                                             ctypes.c_int]
@@ -174,6 +176,17 @@ def qk_pages_f16(Q, K, current_pos, threads: int = 0) -> np.ndarray:
                                S, _ptr(cp, ctypes.c_uint32), _ptr(out, ctypes.c_uint16),
                                threads)
     return out.view(np.float16)
+
+
+def softmax_f64(x, threads: int = 0) -> np.ndarray:
+    """Row softmax over the last dimension of a float32 [rows, cols] array, fp64."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    if a.ndim != 2:
+        raise ValueError(f"x must be [rows, cols], got {a.shape}")
+    out = np.empty(a.shape, dtype=np.float64)
+    _lib().oracle_softmax_f64(_ptr(a, ctypes.c_float), a.shape[0], a.shape[1],
+                              _ptr(out, ctypes.c_double), threads)
+    return out
 
 
 def f16_bits_to_f64(bits) -> np.ndarray:

@@ -323,6 +323,35 @@ void oracle_qk_pages_f16(const uint16_t *Q, const uint16_t *K, int64_t B,
     }
 }
 
+/*
+ * Row softmax over the last dimension, fp64 (the fm_softmax operation of
+ * Foundry's docs/metal.md: x [rows, cols] -> out [rows, cols]): per row
+ *   out[r, c] = exp(x[r, c] - max_c x[r, c]) / sum_c exp(x[r, c] - max_c x[r, c]).
+ * -infinity entries get weight 0; a row that is all -infinity (or holds a NaN)
+ * gives NaN, as the definition does.
+ */
+void oracle_softmax_f64(const float *x, int64_t rows, int64_t cols, double *out,
+                        int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * cols;
+        double *o = out + r * cols;
+        double M = -INFINITY;
+        int has_nan = 0;
+        for (int64_t c = 0; c < cols; ++c) {
+            if (isnan(xr[c])) has_nan = 1;
+            if ((double)xr[c] > M) M = (double)xr[c];
+        }
+        double den = 0.0;
+        for (int64_t c = 0; c < cols; ++c) {
+            o[c] = exp((double)xr[c] - M);
+            den += o[c];
+        }
+        for (int64_t c = 0; c < cols; ++c) o[c] = has_nan ? NAN : o[c] / den;
+    }
+}
+
 /* Vectorised helpers for the tests that pin the conversions themselves. */
 void oracle_f16_to_f64_array(const uint16_t *in, double *out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_f16_to_f64(in[i]);

@@ -48,6 +48,8 @@ MUTANTS = [
      "const uint16_t *k = K_pages + ((pg * page_size + p / page_size) * H + h) * D;", 1),
     ("paged_v_page_of_k", "const uint16_t *v = V_pages + ((pg * page_size + p % page_size) * H + h) * D;",
      "const uint16_t *v = V_pages + ((pg + p % page_size) * H + h) * D;", 1),
+    ("softmax_no_normalisation", "for (int64_t c = 0; c < cols; ++c) o[c] = has_nan ? NAN : o[c] / den;",
+     "for (int64_t c = 0; c < cols; ++c) o[c] = has_nan ? NAN : o[c];", 1),
     ("pv_v_transposed", "const uint16_t *v = V + ((b * S + p) * H + h) * D;\n"
      "                const double wp",
      "const uint16_t *v = V + ((b * H + h) * S + p) * D;\n                const double wp", 1),
@@ -72,6 +74,7 @@ def _pin_checks():
         ("pv_closed", pins.test_pv_closed_forms),
         ("qk_square", pins.test_qk_f64_square_head_dims_exact),
         ("paged_identity", pins.test_paged_identity_table_equals_dense),
+        ("softmax_torch", pins.test_softmax_matches_torch_fp64),
         ("paged_random", lambda: pins.test_paged_random_and_shared_tables_equal_dense_gather(5)),
     ]
 

@@ -417,3 +417,39 @@ def test_paged_invalid_live_page_gives_nan_row_only_for_that_sequence():
     got = oracle.decode_paged_f64(Q, Kp, Vp, table, cp)
     assert np.isnan(got[1]).all()
     assert np.array_equal(got[[0, 2]], good[[0, 2]])
+
+
+# ---------------------------------------------------------- row softmax
+
+def test_softmax_matches_torch_fp64():
+    rng = np.random.default_rng(50)
+    x = (rng.standard_normal((37, 129)) * 6).astype(np.float32)
+    x[3, ::2] = -np.inf
+    x[5, :] = -np.inf
+    x[5, 7] = 2.0
+    ref = torch.softmax(torch.from_numpy(x.astype(np.float64)), dim=-1).numpy()
+    np.testing.assert_allclose(oracle.softmax_f64(x), ref, rtol=1e-13, atol=1e-300)
+
+
+def test_softmax_closed_forms_and_invariants():
+    rng = np.random.default_rng(51)
+    # constant row: uniform weights
+    assert np.array_equal(oracle.softmax_f64(np.full((2, 8), 3.5, np.float32)),
+                          np.full((2, 8), 1 / 8))
+    # shifting a row changes nothing (up to rounding); rows sum to one
+    x = rng.standard_normal((6, 50)).astype(np.float32)
+    a = oracle.softmax_f64(x)
+    b = oracle.softmax_f64(x + np.float32(1000.0))
+    np.testing.assert_allclose(a, b, rtol=1e-4, atol=0)  # x + 1000 rounds in float32
+    np.testing.assert_allclose(a.sum(axis=1), 1.0, rtol=1e-14)
+    # two entries: a sigmoid of their difference
+    y = np.array([[0.25, -1.5]], np.float32)
+    d = float(y[0, 0]) - float(y[0, 1])
+    np.testing.assert_allclose(oracle.softmax_f64(y)[0],
+                               [1 / (1 + math.exp(-d)), 1 / (1 + math.exp(d))], rtol=1e-15)
+    # all -inf or a NaN gives NaN for that row only
+    z = rng.standard_normal((3, 4)).astype(np.float32)
+    z[0] = -np.inf
+    z[2, 1] = np.nan
+    o = oracle.softmax_f64(z)
+    assert np.isnan(o[0]).all() and np.isnan(o[2]).all() and np.isfinite(o[1]).all()
