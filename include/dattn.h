@@ -236,6 +236,19 @@ int dattn_decode_f16_noalloc(const void *Q, const void *K_cache, const void *V_c
                              const uint32_t *current_pos, dattn_stream_t stream);
 
 /*
+ * Row softmax over the last dimension, f32: the fm_softmax operation of the C
+ * API in Foundry's docs/metal.md ("Custom Compute Kernels"), i.e. the
+ * max-subtracted softmax of the decode path's reduction on its own:
+ *   out[r, c] = exp(x[r, c] - max_c x[r, c]) / sum_c exp(x[r, c] - max_c x[r, c])
+ *   x, out  [rows, cols] f32, device, row-major, 4-byte aligned (out may equal x)
+ * computed in fp32 (expf).  -infinity entries get weight 0; a row with a NaN,
+ * or with every entry -infinity, comes out NaN, as the definition gives.
+ * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED, CUDA.
+ */
+int dattn_softmax_f32(const float *x, float *out, long long rows, int cols,
+                      dattn_stream_t stream);
+
+/*
  * Submission batching: the analogue of the fm_batch_begin / fm_batch_end pair
  * of the C API in Foundry's docs/metal.md (section "Command Batching"), which
  * accumulates operations into one GPU submission.  Here the calls issued on a

@@ -129,3 +129,10 @@ def test_batch_api_rejects_bad_arguments_on_host(lib):
     assert lib.dattn_batch_launch(None, None) == _native.ERR_INVALID_ARG
     assert lib.dattn_batch_nodes(None) == -1
     assert lib.dattn_batch_destroy(None) == _native.OK
+
+
+def test_softmax_rejects_bad_arguments_on_host(lib):
+    assert lib.dattn_softmax_f32(None, A, 4, 8, None) == _native.ERR_INVALID_ARG
+    assert lib.dattn_softmax_f32(A + 2, A, 4, 8, None) == _native.ERR_MISALIGNED
+    assert lib.dattn_softmax_f32(A, A, 0, 8, None) == _native.ERR_INVALID_ARG
+    assert lib.dattn_softmax_f32(A, A, 4, -1, None) == _native.ERR_INVALID_ARG

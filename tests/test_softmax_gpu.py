@@ -1,0 +1,72 @@
+"""Standalone row softmax (dattn_softmax_f32) against the fp64 oracle."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import token_decode_attention_gb300 as dattn
+
+pytestmark = pytest.mark.gpu
+
+# fp32 with expf: per element about 1e-6 relative; the row sum adds at most a
+# few 1e-6 for the widths below.  Bound: |out - ref| <= 1e-7 + 2e-5 |ref|.
+ATOL, RTOL = 1e-7, 2e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from token_decode_attention_gb300 import build
+    build.build()
+    dattn.load()
+
+
+def check(x: torch.Tensor, out: torch.Tensor):
+    ref = oracle.softmax_f64(x.cpu().numpy())
+    got = out.cpu().numpy().astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    err = np.abs(got[~nan] - ref[~nan])
+    assert (err <= ATOL + RTOL * np.abs(ref[~nan])).all(), f"max err {err.max():.3g}"
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 1), (7, 5), (64, 32), (33, 1000), (5, 1024),
+                                       (9, 1025), (4, 4096), (3, 8191), (2, 131072)])
+def test_softmax_matches_oracle(rows, cols):
+    g = torch.Generator(device="cuda").manual_seed(rows * 100003 + cols)
+    x = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+    x.normal_(0.0, 4.0, generator=g)
+    out = dattn.softmax(x)
+    torch.cuda.synchronize()
+    check(x, out)
+
+
+def test_softmax_masked_and_degenerate_rows():
+    g = torch.Generator(device="cuda").manual_seed(3)
+    for cols in (300, 5000):  # one warp per row, one CTA per row
+        x = torch.empty((6, cols), dtype=torch.float32, device="cuda")
+        x.normal_(0.0, 3.0, generator=g)
+        x[0, ::3] = float("-inf")          # masked entries: weight 0
+        x[1] = float("-inf")               # all masked: NaN row
+        x[2, 5] = float("nan")             # a NaN: NaN row
+        x[3, 0] = float("-inf")
+        x[3, 1:] = float("-inf")
+        x[3, 7] = float("nan")             # -inf first, then a NaN: NaN row
+        x[4] = 7.0                         # constant: uniform
+        x[5] += 1000.0                     # large values: max subtraction
+        out = dattn.softmax(x)
+        torch.cuda.synchronize()
+        check(x, out)
+        assert float(out[0, 0]) == 0.0
+
+
+def test_softmax_in_place_and_row_sums():
+    g = torch.Generator(device="cuda").manual_seed(4)
+    x = torch.empty((100, 2048), dtype=torch.float32, device="cuda")
+    x.normal_(0.0, 2.0, generator=g)
+    ref = x.clone()
+    dattn.dattn_softmax_f32(x, x)  # out may equal x
+    torch.cuda.synchronize()
+    check(ref, x)
+    assert torch.allclose(x.double().sum(dim=1), torch.ones(100, dtype=torch.float64), atol=1e-5)

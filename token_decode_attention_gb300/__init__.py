@@ -18,10 +18,12 @@ from ._native import (  # noqa: F401
     dattn_device_error,
     dattn_pv_f16,
     dattn_qk_f16,
+    dattn_softmax_f32,
     dattn_version,
     decode,
     decode_paged,
     load,
     pv,
     qk,
+    softmax,
 )

@@ -59,6 +59,7 @@ _SIGNATURES = {
     "dattn_pv_f16": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
     "dattn_device_error": ([_I], _I),
     "dattn_selftest_wait_timeout": ([_P], _I),
+    "dattn_softmax_f32": ([_P, _P, ctypes.c_longlong, _I, _P], _I),
     "dattn_batch_begin": ([_P], _I),
     "dattn_batch_end": ([_P, ctypes.POINTER(ctypes.c_void_p)], _I),
     "dattn_batch_launch": ([_P, _P], _I),
@@ -229,6 +230,23 @@ def dattn_device_error(clear: bool = True) -> int:
     if st not in (OK, ERR_TIMEOUT, ERR_BAD_PAGE):
         _check(st, "dattn_device_error")
     return st
+
+
+def dattn_softmax_f32(x, out, stream=None) -> None:
+    if x.dim() != 2:
+        raise ValueError("x must be [rows, cols]")
+    rows, cols = (int(v) for v in x.shape)
+    _check(load().dattn_softmax_f32(_tensor(x, "x", (rows, cols), torch.float32),
+                                    _tensor(out, "out", (rows, cols), torch.float32), rows, cols,
+                                    _stream_handle(stream)), "dattn_softmax_f32")
+
+
+def softmax(x, out=None, stream=None):
+    """Row softmax over the last dimension of a float32 [rows, cols] tensor."""
+    if out is None:
+        out = torch.empty_like(x)
+    dattn_softmax_f32(x, out, stream)
+    return out
 
 
 def dattn_selftest_wait_timeout(stream=None) -> None:

@@ -552,6 +552,22 @@ int dattn_pv_f16(const void *scores, const void *V_cache, void *out, int batch, 
     return e == cudaSuccess ? DATTN_OK : fail_cuda(e, "pv kernel launch");
 }
 
+int dattn_softmax_f32(const float *x, float *out, long long rows, int cols,
+                      dattn_stream_t stream) {
+    if (x == nullptr || out == nullptr) return fail(DATTN_ERR_INVALID_ARG, "x or out is NULL");
+    if ((reinterpret_cast<uintptr_t>(x) & 3u) || (reinterpret_cast<uintptr_t>(out) & 3u))
+        return fail(DATTN_ERR_MISALIGNED, "x and out must be 4-byte aligned");
+    if (rows <= 0 || cols <= 0)
+        return fail(DATTN_ERR_INVALID_ARG, "rows=%lld and cols=%d must be positive", rows, cols);
+    if (static_cast<double>(rows) * cols > 4.0e18)
+        return fail(DATTN_ERR_INVALID_ARG, "matrix is too large");
+    if (cols > 1024 && rows > 0x7fffffffLL)
+        return fail(DATTN_ERR_UNSUPPORTED, "at most 2^31-1 rows of more than 1024 columns");
+    const cudaError_t e =
+        dattn::launch_softmax(x, out, rows, cols, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DATTN_OK : fail_cuda(e, "softmax kernel launch");
+}
+
 int dattn_selftest_wait_timeout(dattn_stream_t stream) {
     DeviceInfo di;
     if (int st = device_info(&di)) return st;

@@ -103,6 +103,10 @@ int set_last_error(int status, const char *message);
 // nothing arrives on and records kErrSelftestWait in `err` when the wait runs out.
 cudaError_t launch_wait_timeout_selftest(unsigned *err, cudaStream_t stream);
 
+// Row softmax over the last dimension of a f32 [rows, cols] matrix.
+cudaError_t launch_softmax(const float *x, float *out, long long rows, int cols,
+                           cudaStream_t stream);
+
 // Page-faithful split calls.
 cudaError_t launch_qk(const void *Q, const void *K, void *scores, int B, int H, int D, int S,
                       const uint32_t *cur_pos, cudaStream_t stream);
