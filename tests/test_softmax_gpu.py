@@ -69,4 +69,5 @@ def test_softmax_in_place_and_row_sums():
     dattn.dattn_softmax_f32(x, x)  # out may equal x
     torch.cuda.synchronize()
     check(ref, x)
-    assert torch.allclose(x.double().sum(dim=1), torch.ones(100, dtype=torch.float64), atol=1e-5)
+    assert torch.allclose(x.double().sum(dim=1).cpu(), torch.ones(100, dtype=torch.float64),
+                          atol=1e-5)
