@@ -40,6 +40,8 @@ def _load(path: str):
     lib.oracle_f16_to_f64_array.argtypes = [u16p, f64p, i64]
     lib.oracle_f32_to_f16_array.argtypes = [ctypes.POINTER(ctypes.c_float), u16p, i64]
     lib.oracle_max_threads.restype = ctypes.c_int
+    lib.oracle_rope_f64.argtypes = [u16p, i64, i64, i64, i64, ctypes.c_double, ctypes.c_int,
+                                    u32p, f64p]
     lib.oracle_softmax_f64.argtypes = [ctypes.POINTER(ctypes.c_float), i64, i64, f64p,
                                        ctypes.c_int]
     lib.oracle_decode_paged_f64.argtypes = [u16p, u16p, u16p, i64, i64, i64, i64, i64,
@@ -176,6 +178,22 @@ def qk_pages_f16(Q, K, current_pos, threads: int = 0) -> np.ndarray:
                                S, _ptr(cp, ctypes.c_uint32), _ptr(out, ctypes.c_uint16),
                                threads)
     return out.view(np.float16)
+
+
+def rope_f64(x, position, rope_dims: int | None = None, base: float = 10000.0,
+             traditional: bool = False) -> np.ndarray:
+    """Rotary embedding of x [B,H,D] float16 at per-sequence positions, fp64."""
+    a = _f16_bits(x, 3, "x")
+    B, H, D = a.shape
+    rd = D if rope_dims is None else int(rope_dims)
+    if rd < 2 or rd > D or rd % 2:
+        raise ValueError(f"rope_dims must be even and in [2, {D}], got {rd}")
+    pos = _cur_pos(position, B)
+    out = np.empty((B, H, D), dtype=np.float64)
+    _lib().oracle_rope_f64(_ptr(a, ctypes.c_uint16), B, H, D, rd, float(base),
+                           1 if traditional else 0, _ptr(pos, ctypes.c_uint32),
+                           _ptr(out, ctypes.c_double))
+    return out
 
 
 def softmax_f64(x, threads: int = 0) -> np.ndarray:

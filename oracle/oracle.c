@@ -352,6 +352,39 @@ void oracle_softmax_f64(const float *x, int64_t rows, int64_t cols, double *out,
     }
 }
 
+/*
+ * Rotary position embedding of one token per sequence, fp64 ("Tutorial 16:
+ * Writing Custom Metal Kernels", section 5, FastRoPE: vectors split into pairs,
+ * a 2D rotation of each pair by an angle set by the position, the position
+ * offset given per batch entry).  For sequence b at position pos_b and pair i
+ * (i < rope_dims / 2), theta_i = base^(-2 i / rope_dims) and a = pos_b * theta_i:
+ *   non-traditional (default): the pair is (x[i], x[i + rope_dims/2]);
+ *   traditional:               the pair is (x[2i], x[2i + 1]);
+ *   (u, w) -> (u cos a - w sin a, u sin a + w cos a).
+ * Channels from rope_dims on are copied unchanged.
+ * x [B, H, D] f16 -> out [B, H, D] fp64.
+ */
+void oracle_rope_f64(const uint16_t *x, int64_t B, int64_t H, int64_t D, int64_t rope_dims,
+                     double base, int traditional, const uint32_t *position, double *out) {
+    const int64_t half = rope_dims / 2;
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t h = 0; h < H; ++h) {
+            const uint16_t *xv = x + (b * H + h) * D;
+            double *o = out + (b * H + h) * D;
+            for (int64_t d = 0; d < D; ++d) o[d] = oracle_f16_to_f64(xv[d]);
+            for (int64_t i = 0; i < half; ++i) {
+                const double theta = pow(base, -2.0 * (double)i / (double)rope_dims);
+                const double a = (double)position[b] * theta;
+                const int64_t i0 = traditional ? 2 * i : i;
+                const int64_t i1 = traditional ? 2 * i + 1 : i + half;
+                const double u = oracle_f16_to_f64(xv[i0]), w = oracle_f16_to_f64(xv[i1]);
+                o[i0] = u * cos(a) - w * sin(a);
+                o[i1] = u * sin(a) + w * cos(a);
+            }
+        }
+    }
+}
+
 /* Vectorised helpers for the tests that pin the conversions themselves. */
 void oracle_f16_to_f64_array(const uint16_t *in, double *out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_f16_to_f64(in[i]);

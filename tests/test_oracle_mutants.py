@@ -50,6 +50,9 @@ MUTANTS = [
      "const uint16_t *v = V_pages + ((pg + p % page_size) * H + h) * D;", 1),
     ("softmax_no_normalisation", "for (int64_t c = 0; c < cols; ++c) o[c] = has_nan ? NAN : o[c] / den;",
      "for (int64_t c = 0; c < cols; ++c) o[c] = has_nan ? NAN : o[c];", 1),
+    ("rope_sin_sign", "o[i0] = u * cos(a) - w * sin(a);", "o[i0] = u * cos(a) + w * sin(a);", 1),
+    ("rope_theta_exponent", "const double theta = pow(base, -2.0 * (double)i / (double)rope_dims);",
+     "const double theta = pow(base, -1.0 * (double)i / (double)rope_dims);", 1),
     ("pv_v_transposed", "const uint16_t *v = V + ((b * S + p) * H + h) * D;\n"
      "                const double wp",
      "const uint16_t *v = V + ((b * H + h) * S + p) * D;\n                const double wp", 1),
@@ -75,6 +78,7 @@ def _pin_checks():
         ("qk_square", pins.test_qk_f64_square_head_dims_exact),
         ("paged_identity", pins.test_paged_identity_table_equals_dense),
         ("softmax_torch", pins.test_softmax_matches_torch_fp64),
+        ("rope_complex", lambda: pins.test_rope_equals_complex_rotation(False, 64)),
         ("paged_random", lambda: pins.test_paged_random_and_shared_tables_equal_dense_gather(5)),
     ]
 

@@ -453,3 +453,63 @@ def test_softmax_closed_forms_and_invariants():
     z[2, 1] = np.nan
     o = oracle.softmax_f64(z)
     assert np.isnan(o[0]).all() and np.isnan(o[2]).all() and np.isfinite(o[1]).all()
+
+
+# ------------------------------------------------------- rotary embedding
+
+def _rope_complex(x64, pos, rd, base, traditional):
+    # the same rotation as complex multiplication by exp(i a), with numpy
+    B, H, D = x64.shape
+    half = rd // 2
+    theta = base ** (-2.0 * np.arange(half) / rd)
+    a = np.asarray(pos, np.float64)[:, None, None] * theta[None, None, :]
+    if traditional:
+        z = x64[..., 0:rd:2] + 1j * x64[..., 1:rd:2]
+    else:
+        z = x64[..., :half] + 1j * x64[..., half:rd]
+    z = z * np.exp(1j * a)
+    out = x64.copy()
+    if traditional:
+        out[..., 0:rd:2], out[..., 1:rd:2] = z.real, z.imag
+    else:
+        out[..., :half], out[..., half:rd] = z.real, z.imag
+    return out
+
+
+@pytest.mark.parametrize("traditional", [False, True])
+@pytest.mark.parametrize("rd", [8, 64, 128])
+def test_rope_equals_complex_rotation(traditional, rd):
+    rng = np.random.default_rng(60 + rd)
+    x = rand_f16(rng, (3, 4, 128))
+    pos = np.array([0, 17, 131071], np.uint32)
+    got = oracle.rope_f64(x, pos, rd, 10000.0, traditional)
+    ref = _rope_complex(x.astype(np.float64), pos, rd, 10000.0, traditional)
+    np.testing.assert_allclose(got, ref, rtol=1e-9, atol=1e-9)
+
+
+def test_rope_position_zero_is_identity_and_norms_are_kept():
+    # the page-1 engine's RoPE tests: position zero is the identity, and
+    # different positions differ; a rotation keeps each pair's norm
+    rng = np.random.default_rng(61)
+    x = rand_f16(rng, (2, 3, 64))
+    assert np.array_equal(oracle.rope_f64(x, [0, 0]), x.astype(np.float64))
+    r = oracle.rope_f64(x, [5, 900])
+    assert not np.allclose(r, x.astype(np.float64))
+    x64 = x.astype(np.float64)
+    np.testing.assert_allclose(r[..., :32] ** 2 + r[..., 32:] ** 2,
+                               x64[..., :32] ** 2 + x64[..., 32:] ** 2, rtol=1e-12)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    rng = np.random.default_rng(62)
+    q, k = rand_f16(rng, (1, 1, 64)), rand_f16(rng, (1, 1, 64))
+    s1 = float((oracle.rope_f64(q, [100]) * oracle.rope_f64(k, [40])).sum())
+    s2 = float((oracle.rope_f64(q, [1060]) * oracle.rope_f64(k, [1000])).sum())
+    assert abs(s1 - s2) <= 1e-9 * max(1.0, abs(s1))
+
+
+def test_rope_leaves_channels_past_rope_dims_unchanged():
+    rng = np.random.default_rng(63)
+    x = rand_f16(rng, (2, 2, 96))
+    r = oracle.rope_f64(x, [7, 3000], rope_dims=32)
+    assert np.array_equal(r[..., 32:], x[..., 32:].astype(np.float64))
