@@ -36,7 +36,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from token_decode_attention_gb300.workloads import (  # noqa: E402
-    WORKLOADS, algorithmic_bytes, make_inputs)
+    WORKLOADS, algorithmic_bytes, draw_current_pos, make_inputs)
 
 METRIC = "decode-attention effective HBM GB/s (% of GB300 peak) and query-heads/s"
 NOMINAL_HBM_GBS = 8000.0
@@ -308,8 +308,9 @@ class Replica:
     def e2e(self, steps: int, warmup: int, stream):
         """Same metric through the public API with host buffers: each step copies
         Q, the new token's K/V row and current_pos from pinned host memory,
-        appends the K/V row at current_pos, runs the decode and reads out back
-        into pinned host memory.  The KV cache itself is device-resident state."""
+        rotates q and k at current_pos and appends k, v to the cache
+        (dattn_rope_append_f16), runs the decode and reads out back into pinned
+        host memory.  The KV cache itself is device-resident state."""
         if self.page_size:
             return None  # measured on the dense layout only
         w = self.w
@@ -325,9 +326,6 @@ class Replica:
         cp_d = torch.empty_like(x["cur_pos"])
         knew_d = torch.empty((B, H, D), dtype=torch.float16, device=self.device)
         vnew_d = torch.empty_like(knew_d)
-        rows = torch.from_numpy(np.arange(B) * w.seq_len + last).to(self.device)
-        kflat = x["k"].view(B * w.seq_len, H, D)
-        vflat = x["v"].view(B * w.seq_len, H, D)
         out_d = self.outs[0]
         h2d = (q_h.numel() + knew_h.numel() + vnew_h.numel()) * 2 + cp_h.numel() * 4
         d2h = out_h.numel() * 2
@@ -339,8 +337,8 @@ class Replica:
             cp_d.copy_(cp_h, non_blocking=True)
             knew_d.copy_(knew_h, non_blocking=True)
             vnew_d.copy_(vnew_h, non_blocking=True)
-            kflat.index_copy_(0, rows, knew_d)
-            vflat.index_copy_(0, rows, vnew_d)
+            self.dattn.dattn_rope_append_f16(q_d, knew_d, vnew_d, q_d, x["k"], x["v"], cp_d,
+                                             stream=stream)
             self.dattn.dattn_decode_f16_ex(q_d, x["k"], x["v"], out_d, cp_d, self.ws,
                                            self.partitions, stream)
             out_h.copy_(out_d, non_blocking=True)
@@ -362,9 +360,95 @@ class Replica:
         return {"value": self.bytes_per_step / (ms * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": ms, "wall_ms_per_step": wall * 1e3 / steps,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "launches_per_step": 1 + self.launches_per_step,
                 "note": "Q, new K/V row and current_pos copied H2D from pinned memory, "
-                        "K/V row appended at current_pos, decode, out copied D2H; "
-                        "the KV cache is device-resident state"}
+                        "q and k rotated and K/V row appended at current_pos "
+                        "(dattn_rope_append_f16), decode, out copied D2H; the KV cache is "
+                        "device-resident state; value counts the decode's bytes only"}
+
+
+def graph_time_us(fn, steps: int, warmup: int, stream) -> float:
+    """Device time per call of `fn(i, stream)`: `steps` calls captured in one
+    CUDA graph, replayed once between two events on `stream`."""
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            fn(i, stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(steps):
+                fn(i, stream)
+        g.replay()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        g.replay()
+        end.record(stream)
+        torch.cuda.synchronize()
+    return start.elapsed_time(end) * 1e3 / steps
+
+
+def sweep_ops(device, stream, steps: int, warmup: int, peak: float) -> dict:
+    """The two other kernels of a decode step, each timed alone.
+
+    rope_append: rotate the new q and k and append k, v at current_pos, for the
+    decode shapes of the 7b, ragged and outlier workloads; algorithmic bytes
+    3 B H D halves read + 3 B H D halves written + current_pos.  The inputs are
+    small and L2-resident: these are launch/latency figures.
+    softmax: f32 row softmax, 8 bytes per element (one read, one write), inputs
+    larger than L2, rotating two input sets."""
+    import token_decode_attention_gb300 as dattn
+    res = {}
+    for name in ("7b", "ragged", "outlier"):
+        w = WORKLOADS[name]
+        B, H, D, S = w.batch, w.n_heads, w.head_dim, w.seq_len
+        try:
+            g = torch.Generator(device=device).manual_seed(w.seed)
+            new = [torch.empty((B, H, D), dtype=torch.float16, device=device).normal_(
+                generator=g) for _ in range(3)]
+            qo = torch.empty_like(new[0])
+            # a cache of 8 positions per sequence is enough: only row cp is touched
+            cache_s = 8
+            K = torch.zeros((B, cache_s, H, D), dtype=torch.float16, device=device)
+            V = torch.zeros_like(K)
+            cp = torch.from_numpy(
+                (draw_current_pos(w) % cache_s).astype(np.int64)).to(torch.int32).to(device)
+            torch.cuda.synchronize()
+            us = graph_time_us(lambda i, st: dattn.dattn_rope_append_f16(
+                new[0], new[1], new[2], qo, K, V, cp, stream=st), steps, warmup, stream)
+            nbytes = 6 * B * H * D * 2 + 4 * B
+            res[f"rope_append_{name}"] = {"us_per_call": us, "GB/s": nbytes / us / 1e3,
+                                          "algorithmic_bytes": nbytes,
+                                          "shape": f"B={B} H={H} D={D}"}
+            del new, qo, K, V
+        except Exception as e:
+            import traceback
+            traceback.print_exc(file=sys.stderr)
+            res[f"rope_append_{name}"] = {"error": f"{type(e).__name__}: {e}"}
+    for rows, cols in ((10240, 8192), (65536, 1024)):
+        key = f"softmax_{rows}x{cols}"
+        try:
+            g = torch.Generator(device=device).manual_seed(rows + cols)
+            xs = [torch.empty((rows, cols), dtype=torch.float32, device=device).normal_(
+                0.0, 3.0, generator=g) for _ in range(2)]
+            ys = [torch.empty_like(x) for x in xs]
+            torch.cuda.synchronize()
+            us = graph_time_us(lambda i, st: dattn.dattn_softmax_f32(xs[i % 2], ys[i % 2], st),
+                               steps, warmup, stream)
+            nbytes = 8 * rows * cols
+            gbs = nbytes / us / 1e3
+            res[key] = {"us_per_call": us, "GB/s": gbs, "frac_of_measured": gbs / peak,
+                        "algorithmic_bytes": nbytes,
+                        "l2": f"2 input sets of {rows * cols * 4 / 2**20:.0f} MiB"}
+            del xs, ys
+        except Exception as e:
+            import traceback
+            traceback.print_exc(file=sys.stderr)
+            res[key] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.empty_cache()
+    return res
 
 
 def cpu_baseline(name: str, budget_s: float, max_reps: int = 1000) -> dict:
@@ -557,6 +641,7 @@ def main():
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
         if not args.no_sweep:
             line["sweep"] = sweep(device, stream, l2, 20, 3, peak)
+            line["sweep_ops"] = sweep_ops(device, stream, 20, 3, peak)
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -55,7 +55,8 @@ enum dattn_status {
     DATTN_ERR_WORKSPACE = -4,   /* workspace missing, misaligned or too small       */
     DATTN_ERR_CUDA = -5,        /* a CUDA runtime call or kernel launch failed      */
     DATTN_ERR_TIMEOUT = -6,     /* a kernel gave up waiting on its own pipeline     */
-    DATTN_ERR_BAD_PAGE = -7     /* a live position's block-table entry was invalid  */
+    DATTN_ERR_BAD_PAGE = -7,    /* a live position's block-table entry was invalid  */
+    DATTN_ERR_BAD_POSITION = -8 /* an append position was outside the cache         */
 };
 
 /* Library version: major*10000 + minor*100 + patch. */
@@ -236,6 +237,41 @@ int dattn_decode_f16_noalloc(const void *Q, const void *K_cache, const void *V_c
                              const uint32_t *current_pos, dattn_stream_t stream);
 
 /*
+ * The step before decode attention: rotary position embedding of the new
+ * token's query and key fused with appending the key and value to the cache
+ * ("Tutorial 16: Writing Custom Metal Kernels", section 5: FastRoPE splits each
+ * vector into pairs and rotates every pair by a position-dependent angle, with
+ * one position offset per batch entry).  For sequence b the new token sits at
+ * position p = current_pos[b]; for pair i < rope_dims/2,
+ *   theta_i = rope_base^(-2 i / rope_dims),  a = p * theta_i  (in fp64),
+ *   pair (i, i + rope_dims/2), or (2i, 2i+1) when `traditional` is non-zero,
+ *   (u, w) -> (u cos a - w sin a, u sin a + w cos a)  (fp32, rounded to f16);
+ *   channels from rope_dims on are copied.
+ * Writes q_out[b,h,:] = rope(q_new[b,h,:]) (q_out may be q_new),
+ *        K_cache[b,p,h,:] = rope(k_new[b,h,:]),  V_cache[b,p,h,:] = v_new[b,h,:].
+ *   q_new, k_new, v_new, q_out  [batch, n_heads, head_dim] f16, device
+ *   K_cache, V_cache            [batch, seq_len, n_heads, head_dim] f16, device
+ * A position p >= seq_len is not written; dattn_device_error() then reports
+ * DATTN_ERR_BAD_POSITION.  Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, CUDA.
+ */
+int dattn_rope_append_f16(const void *q_new, const void *k_new, const void *v_new, void *q_out,
+                          void *K_cache, void *V_cache, int batch, int n_heads, int head_dim,
+                          int seq_len, int rope_dims, double rope_base, int traditional,
+                          const uint32_t *current_pos, dattn_stream_t stream);
+
+/*
+ * The same over a paged cache (see dattn_decode_paged_f16): the key and value
+ * go to page block_table[b, p / page_size], row p % page_size.  An invalid
+ * page is not written and reported as DATTN_ERR_BAD_PAGE.
+ */
+int dattn_rope_append_paged_f16(const void *q_new, const void *k_new, const void *v_new,
+                                void *q_out, void *K_pages, void *V_pages, int batch,
+                                int n_heads, int head_dim, int page_size, int max_pages,
+                                long long num_pages, const int32_t *block_table, int rope_dims,
+                                double rope_base, int traditional, const uint32_t *current_pos,
+                                dattn_stream_t stream);
+
+/*
  * Row softmax over the last dimension, f32: the fm_softmax operation of the C
  * API in Foundry's docs/metal.md ("Custom Compute Kernels"), i.e. the
  * max-subtracted softmax of the decode path's reduction on its own:
@@ -283,9 +319,10 @@ int dattn_batch_destroy(dattn_batch *batch);
  * of hanging the GPU.  The paged decode records invalid block-table entries
  * here too.  This call synchronises the device and returns DATTN_OK if no
  * kernel has recorded anything since the last clear, DATTN_ERR_TIMEOUT if a
- * wait ran out, DATTN_ERR_BAD_PAGE if only a block-table entry was invalid;
- * it resets the word when `clear` is non-zero.
- * Errors: TIMEOUT, BAD_PAGE, CUDA.
+ * wait ran out, DATTN_ERR_BAD_PAGE if a block-table entry was invalid,
+ * DATTN_ERR_BAD_POSITION if an append position was outside the cache; it
+ * resets the word when `clear` is non-zero.
+ * Errors: TIMEOUT, BAD_PAGE, BAD_POSITION, CUDA.
  */
 int dattn_device_error(int clear);
 

@@ -45,7 +45,7 @@ def test_version_and_status_strings(lib):
     for code, name in [(0, "DATTN_OK"), (-1, "DATTN_ERR_INVALID_ARG"), (-2, "DATTN_ERR_UNSUPPORTED"),
                        (-3, "DATTN_ERR_MISALIGNED"), (-4, "DATTN_ERR_WORKSPACE"),
                        (-5, "DATTN_ERR_CUDA"), (-6, "DATTN_ERR_TIMEOUT"),
-                       (-7, "DATTN_ERR_BAD_PAGE")]:
+                       (-7, "DATTN_ERR_BAD_PAGE"), (-8, "DATTN_ERR_BAD_POSITION")]:
         assert lib.dattn_status_string(code).decode() == name
 
 
@@ -136,3 +136,40 @@ def test_softmax_rejects_bad_arguments_on_host(lib):
     assert lib.dattn_softmax_f32(A + 2, A, 4, 8, None) == _native.ERR_MISALIGNED
     assert lib.dattn_softmax_f32(A, A, 0, 8, None) == _native.ERR_INVALID_ARG
     assert lib.dattn_softmax_f32(A, A, 4, -1, None) == _native.ERR_INVALID_ARG
+
+
+def rope_call(lib, q=A, k=A, v=A, qo=A, K=A, V=A, B=2, H=4, D=64, S=32, rd=64, base=10000.0,
+              cp=A):
+    return lib.dattn_rope_append_f16(q, k, v, qo, K, V, B, H, D, S, rd, base, 0, cp, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), _native.ERR_INVALID_ARG),
+    (dict(V=None), _native.ERR_INVALID_ARG),
+    (dict(k=A + 8), _native.ERR_MISALIGNED),
+    (dict(cp=None), _native.ERR_INVALID_ARG),
+    (dict(cp=A + 2), _native.ERR_MISALIGNED),
+    (dict(B=0), _native.ERR_INVALID_ARG),
+    (dict(S=-1), _native.ERR_INVALID_ARG),
+    (dict(D=20, rd=20), _native.ERR_UNSUPPORTED),
+    (dict(rd=0), _native.ERR_INVALID_ARG),
+    (dict(rd=31), _native.ERR_INVALID_ARG),
+    (dict(rd=66), _native.ERR_INVALID_ARG),
+    (dict(base=1.0), _native.ERR_INVALID_ARG),
+    (dict(base=float("inf")), _native.ERR_INVALID_ARG),
+    (dict(base=float("nan")), _native.ERR_INVALID_ARG),
+])
+def test_rope_append_rejects_bad_arguments_on_host(lib, kw, status):
+    assert rope_call(lib, **kw) == status
+
+
+def test_paged_rope_append_rejects_bad_arguments_on_host(lib):
+    def call(table=A, ps=16, maxp=4, npages=8, rd=64):
+        return lib.dattn_rope_append_paged_f16(A, A, A, A, A, A, 2, 4, 64, ps, maxp, npages,
+                                               table, rd, 10000.0, 1, A, None)
+    assert call(table=None) == _native.ERR_INVALID_ARG
+    assert call(table=A + 2) == _native.ERR_MISALIGNED
+    assert call(ps=0) == _native.ERR_INVALID_ARG
+    assert call(npages=0) == _native.ERR_INVALID_ARG
+    assert call(ps=1 << 20, maxp=1 << 12) == _native.ERR_UNSUPPORTED
+    assert call(rd=3) == _native.ERR_INVALID_ARG

@@ -18,6 +18,8 @@ from ._native import (  # noqa: F401
     dattn_device_error,
     dattn_pv_f16,
     dattn_qk_f16,
+    dattn_rope_append_f16,
+    dattn_rope_append_paged_f16,
     dattn_softmax_f32,
     dattn_version,
     decode,
@@ -25,5 +27,6 @@ from ._native import (  # noqa: F401
     load,
     pv,
     qk,
+    rope_append,
     softmax,
 )

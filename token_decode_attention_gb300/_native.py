@@ -39,7 +39,7 @@ class Plan(ctypes.Structure):
 
 # status codes (enum dattn_status)
 (OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT,
- ERR_BAD_PAGE) = (0, -1, -2, -3, -4, -5, -6, -7)
+ ERR_BAD_PAGE, ERR_BAD_POSITION) = (0, -1, -2, -3, -4, -5, -6, -7, -8)
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -60,6 +60,10 @@ _SIGNATURES = {
     "dattn_device_error": ([_I], _I),
     "dattn_selftest_wait_timeout": ([_P], _I),
     "dattn_softmax_f32": ([_P, _P, ctypes.c_longlong, _I, _P], _I),
+    "dattn_rope_append_f16": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_double, _I,
+                               _P, _P], _I),
+    "dattn_rope_append_paged_f16": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                     ctypes.c_longlong, _P, _I, ctypes.c_double, _I, _P, _P], _I),
     "dattn_batch_begin": ([_P], _I),
     "dattn_batch_end": ([_P, ctypes.POINTER(ctypes.c_void_p)], _I),
     "dattn_batch_launch": ([_P, _P], _I),
@@ -224,10 +228,10 @@ def dattn_pv_f16(scores, v, out, stream=None) -> None:
 
 
 def dattn_device_error(clear: bool = True) -> int:
-    """Status of the device error word (DATTN_OK or DATTN_ERR_TIMEOUT); never raises on
-    TIMEOUT, so callers can assert on it."""
+    """Status of the device error word (DATTN_OK, or the TIMEOUT, BAD_PAGE or
+    BAD_POSITION it records); never raises on those, so callers can assert on it."""
     st = int(load().dattn_device_error(1 if clear else 0))
-    if st not in (OK, ERR_TIMEOUT, ERR_BAD_PAGE):
+    if st not in (OK, ERR_TIMEOUT, ERR_BAD_PAGE, ERR_BAD_POSITION):
         _check(st, "dattn_device_error")
     return st
 
@@ -247,6 +251,58 @@ def softmax(x, out=None, stream=None):
         out = torch.empty_like(x)
     dattn_softmax_f32(x, out, stream)
     return out
+
+
+def dattn_rope_append_f16(q_new, k_new, v_new, q_out, k_cache, v_cache, current_pos,
+                          rope_dims: int = 0, rope_base: float = 10000.0,
+                          traditional: bool = False, stream=None) -> None:
+    if q_new.dim() != 3 or k_cache.dim() != 4:
+        raise ValueError("q_new must be [batch, n_heads, head_dim], the cache [batch, seq_len, "
+                         "n_heads, head_dim]")
+    B, H, D = (int(x) for x in q_new.shape)
+    S = int(k_cache.shape[1])
+    new = [_tensor(t, n, (B, H, D)) for t, n in ((q_new, "q_new"), (k_new, "k_new"),
+                                                 (v_new, "v_new"), (q_out, "q_out"))]
+    _check(load().dattn_rope_append_f16(*new, _tensor(k_cache, "K_cache", (B, S, H, D)),
+                                        _tensor(v_cache, "V_cache", (B, S, H, D)), B, H, D, S,
+                                        rope_dims or D, float(rope_base), int(bool(traditional)),
+                                        _cur_pos(current_pos, B), _stream_handle(stream)),
+           "dattn_rope_append_f16")
+
+
+def dattn_rope_append_paged_f16(q_new, k_new, v_new, q_out, k_pages, v_pages, block_table,
+                                current_pos, rope_dims: int = 0, rope_base: float = 10000.0,
+                                traditional: bool = False, stream=None) -> None:
+    if q_new.dim() != 3 or k_pages.dim() != 4 or block_table.dim() != 2:
+        raise ValueError("q_new must be [batch, n_heads, head_dim], pages [num_pages, page_size, "
+                         "n_heads, head_dim], block_table [batch, max_pages]")
+    B, H, D = (int(x) for x in q_new.shape)
+    num_pages, page_size = int(k_pages.shape[0]), int(k_pages.shape[1])
+    max_pages = int(block_table.shape[1])
+    new = [_tensor(t, n, (B, H, D)) for t, n in ((q_new, "q_new"), (k_new, "k_new"),
+                                                 (v_new, "v_new"), (q_out, "q_out"))]
+    _check(load().dattn_rope_append_paged_f16(
+        *new, _tensor(k_pages, "K_pages", (num_pages, page_size, H, D)),
+        _tensor(v_pages, "V_pages", (num_pages, page_size, H, D)), B, H, D, page_size, max_pages,
+        num_pages, _tensor(block_table, "block_table", (B, max_pages), torch.int32),
+        rope_dims or D, float(rope_base), int(bool(traditional)), _cur_pos(current_pos, B),
+        _stream_handle(stream)), "dattn_rope_append_paged_f16")
+
+
+def rope_append(q_new, k_new, v_new, k_cache, v_cache, current_pos, rope_dims: int = 0,
+                rope_base: float = 10000.0, traditional: bool = False, block_table=None,
+                q_out=None, stream=None):
+    """Rotate the new token's q and k at current_pos[b] and append k, v to the cache
+    (dense, or paged when ``block_table`` is given); returns the rotated q."""
+    if q_out is None:
+        q_out = torch.empty_like(q_new)
+    if block_table is None:
+        dattn_rope_append_f16(q_new, k_new, v_new, q_out, k_cache, v_cache, current_pos,
+                              rope_dims, rope_base, traditional, stream)
+    else:
+        dattn_rope_append_paged_f16(q_new, k_new, v_new, q_out, k_cache, v_cache, block_table,
+                                    current_pos, rope_dims, rope_base, traditional, stream)
+    return q_out
 
 
 def dattn_selftest_wait_timeout(stream=None) -> None:

@@ -379,6 +379,7 @@ const char *dattn_status_string(int status) {
         case DATTN_ERR_CUDA: return "DATTN_ERR_CUDA";
         case DATTN_ERR_TIMEOUT: return "DATTN_ERR_TIMEOUT";
         case DATTN_ERR_BAD_PAGE: return "DATTN_ERR_BAD_PAGE";
+        case DATTN_ERR_BAD_POSITION: return "DATTN_ERR_BAD_POSITION";
         default: return "DATTN_ERR_UNKNOWN";
     }
 }
@@ -552,6 +553,91 @@ int dattn_pv_f16(const void *scores, const void *V_cache, void *out, int batch, 
     return e == cudaSuccess ? DATTN_OK : fail_cuda(e, "pv kernel launch");
 }
 
+namespace {
+int rope_append(const void *q_new, const void *k_new, const void *v_new, void *q_out, void *K,
+                void *V, int batch, int n_heads, int head_dim, int seq_len, int rope_dims,
+                double rope_base, int traditional, const uint32_t *current_pos,
+                const Paging &pg, cudaStream_t stream) {
+    if (int st = check_tensor(q_new, "q_new")) return st;
+    if (int st = check_tensor(k_new, "k_new")) return st;
+    if (int st = check_tensor(v_new, "v_new")) return st;
+    if (int st = check_tensor(q_out, "q_out")) return st;
+    if (int st = check_tensor(K, "K cache")) return st;
+    if (int st = check_tensor(V, "V cache")) return st;
+    if (int st = check_cur_pos(current_pos)) return st;
+    if (int st = validate_dims(batch, n_heads, head_dim, seq_len)) return st;
+    if (rope_dims < 2 || rope_dims > head_dim || rope_dims % 2 != 0)
+        return fail(DATTN_ERR_INVALID_ARG, "rope_dims=%d must be even and in [2, head_dim=%d]",
+                    rope_dims, head_dim);
+    if (!(rope_base > 1.0) || !std::isfinite(rope_base))
+        return fail(DATTN_ERR_INVALID_ARG, "rope_base must be a finite number above 1");
+    DeviceInfo di;
+    if (int st = device_info(&di)) return st;
+    dattn::RopeAppendArgs a{};
+    a.q_new = q_new;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.q_out = q_out;
+    a.K = K;
+    a.V = V;
+    a.block_table = pg.table;
+    a.num_pages = pg.num_pages;
+    a.page_size = pg.page_size;
+    a.max_pages = pg.max_pages;
+    a.cur_pos = current_pos;
+    a.err = di.err_word;
+    a.B = batch;
+    a.H = n_heads;
+    a.D = head_dim;
+    a.S = seq_len;
+    a.rope_dims = rope_dims;
+    a.traditional = traditional ? 1 : 0;
+    for (int i = 0; i < rope_dims / 2; ++i)
+        a.theta[i] = std::pow(rope_base, -2.0 * i / rope_dims);
+    // about two CTAs per SM of work, at most 8 heads per CTA
+    const long long bh = static_cast<long long>(batch) * n_heads;
+    a.heads_per_cta = static_cast<int>(
+        std::max(1LL, std::min(8LL, bh / (2LL * std::max(di.sms, 1)))));
+    const cudaError_t e = dattn::launch_rope_append(a, stream);
+    return e == cudaSuccess ? DATTN_OK : fail_cuda(e, "rope/append kernel launch");
+}
+}  // namespace
+
+int dattn_rope_append_f16(const void *q_new, const void *k_new, const void *v_new, void *q_out,
+                          void *K_cache, void *V_cache, int batch, int n_heads, int head_dim,
+                          int seq_len, int rope_dims, double rope_base, int traditional,
+                          const uint32_t *current_pos, dattn_stream_t stream) {
+    return rope_append(q_new, k_new, v_new, q_out, K_cache, V_cache, batch, n_heads, head_dim,
+                       seq_len, rope_dims, rope_base, traditional, current_pos, Paging(),
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dattn_rope_append_paged_f16(const void *q_new, const void *k_new, const void *v_new,
+                                void *q_out, void *K_pages, void *V_pages, int batch,
+                                int n_heads, int head_dim, int page_size, int max_pages,
+                                long long num_pages, const int32_t *block_table, int rope_dims,
+                                double rope_base, int traditional, const uint32_t *current_pos,
+                                dattn_stream_t stream) {
+    if (block_table == nullptr) return fail(DATTN_ERR_INVALID_ARG, "block_table is NULL");
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0)
+        return fail(DATTN_ERR_MISALIGNED, "block_table is not 4-byte aligned");
+    if (page_size <= 0 || max_pages <= 0 || num_pages <= 0)
+        return fail(DATTN_ERR_INVALID_ARG,
+                    "page_size=%d, max_pages=%d and num_pages=%lld must be positive", page_size,
+                    max_pages, num_pages);
+    const long long cap = static_cast<long long>(page_size) * max_pages;
+    if (cap > 0x7fffffffLL)
+        return fail(DATTN_ERR_UNSUPPORTED, "page_size x max_pages = %lld exceeds 2^31 - 1", cap);
+    Paging pg;
+    pg.table = block_table;
+    pg.num_pages = num_pages;
+    pg.page_size = page_size;
+    pg.max_pages = max_pages;
+    return rope_append(q_new, k_new, v_new, q_out, K_pages, V_pages, batch, n_heads, head_dim,
+                       static_cast<int>(cap), rope_dims, rope_base, traditional, current_pos, pg,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
 int dattn_softmax_f32(const float *x, float *out, long long rows, int cols,
                       dattn_stream_t stream) {
     if (x == nullptr || out == nullptr) return fail(DATTN_ERR_INVALID_ARG, "x or out is NULL");
@@ -640,11 +726,14 @@ int dattn_device_error(int clear) {
         if (e == cudaSuccess) e = cudaDeviceSynchronize();
         if (e != cudaSuccess) return fail_cuda(e, "cudaMemset (error word)");
     }
-    if (word & ~dattn::kErrPageIndex)
+    const unsigned input_bits = dattn::kErrPageIndex | dattn::kErrAppendPosition;
+    if (word & ~input_bits)
         return fail(DATTN_ERR_TIMEOUT, "a kernel gave up on a pipeline wait (code 0x%x)", word);
     if (word & dattn::kErrPageIndex)
         return fail(DATTN_ERR_BAD_PAGE,
                     "a block-table entry of a live position was outside [0, num_pages)");
+    if (word & dattn::kErrAppendPosition)
+        return fail(DATTN_ERR_BAD_POSITION, "an append position was outside the cache");
     return DATTN_OK;
 }
 

@@ -20,6 +20,7 @@ constexpr unsigned kErrProducerWait = 2u;
 constexpr unsigned kErrDrainWait = 4u;
 constexpr unsigned kErrSelftestWait = 8u;
 constexpr unsigned kErrPageIndex = 16u;  // a block-table entry outside [0, num_pages)
+constexpr unsigned kErrAppendPosition = 32u;  // an append position outside the cache
 
 // Time limit of every pipeline wait in the library's kernels.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // one second
@@ -102,6 +103,26 @@ int set_last_error(int status, const char *message);
 // Failure-detection self-test: one CTA waits (bounded) on an mbarrier that
 // nothing arrives on and records kErrSelftestWait in `err` when the wait runs out.
 cudaError_t launch_wait_timeout_selftest(unsigned *err, cudaStream_t stream);
+
+// Arguments of the fused rotary-embedding + KV-append kernel (passed by value;
+// the frequency table travels in the kernel's parameter space).
+constexpr int kRopeMaxPairs = 256;  // rope_dims / 2 for head_dim up to 512
+struct RopeAppendArgs {
+    double theta[kRopeMaxPairs];        // rope_base^(-2 i / rope_dims)
+    const void *q_new, *k_new, *v_new;  // f16 [B,H,D]
+    void *q_out;                        // f16 [B,H,D] (may be q_new)
+    void *K, *V;                        // cache: [B,S,H,D] or pages [num_pages,page_size,H,D]
+    const int *block_table;             // nullptr: dense cache
+    long long num_pages;
+    int page_size, max_pages;
+    const uint32_t *cur_pos;            // [B] position of the new token
+    unsigned *err;
+    int B, H, D, S;
+    int rope_dims;
+    int traditional;
+    int heads_per_cta;
+};
+cudaError_t launch_rope_append(const RopeAppendArgs &a, cudaStream_t stream);
 
 // Row softmax over the last dimension of a f32 [rows, cols] matrix.
 cudaError_t launch_softmax(const float *x, float *out, long long rows, int cols,
