@@ -592,12 +592,18 @@ int rope_append(const void *q_new, const void *k_new, const void *v_new, void *q
     a.S = seq_len;
     a.rope_dims = rope_dims;
     a.traditional = traditional ? 1 : 0;
-    for (int i = 0; i < rope_dims / 2; ++i)
-        a.theta[i] = std::pow(rope_base, -2.0 * i / rope_dims);
-    // about two CTAs per SM of work, at most 8 heads per CTA
+    // theta_i < 1 < 2 pi, so theta_i / (2 pi) is a fraction of a turn below 1/6;
+    // scaled by 2^64 in extended precision it fits in 63 bits.
+    const long double two_pi = 6.283185307179586476925286766559005768L;
+    for (int i = 0; i < rope_dims / 2; ++i) {
+        const double theta = std::pow(rope_base, -2.0 * i / rope_dims);
+        a.turn_frac[i] = static_cast<unsigned long long>(
+            std::llroundl(std::ldexp(static_cast<long double>(theta) / two_pi, 64)));
+    }
+    // about four CTAs per SM of work, at most 8 heads per CTA
     const long long bh = static_cast<long long>(batch) * n_heads;
     a.heads_per_cta = static_cast<int>(
-        std::max(1LL, std::min(8LL, bh / (2LL * std::max(di.sms, 1)))));
+        std::max(1LL, std::min(8LL, bh / (4LL * std::max(di.sms, 1)))));
     const cudaError_t e = dattn::launch_rope_append(a, stream);
     return e == cudaSuccess ? DATTN_OK : fail_cuda(e, "rope/append kernel launch");
 }

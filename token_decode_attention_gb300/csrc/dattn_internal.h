@@ -108,7 +108,9 @@ cudaError_t launch_wait_timeout_selftest(unsigned *err, cudaStream_t stream);
 // the frequency table travels in the kernel's parameter space).
 constexpr int kRopeMaxPairs = 256;  // rope_dims / 2 for head_dim up to 512
 struct RopeAppendArgs {
-    double theta[kRopeMaxPairs];        // rope_base^(-2 i / rope_dims)
+    // theta_i / (2 pi) as a binary fraction in units of 2^-64, theta_i =
+    // rope_base^(-2 i / rope_dims)
+    unsigned long long turn_frac[kRopeMaxPairs];
     const void *q_new, *k_new, *v_new;  // f16 [B,H,D]
     void *q_out;                        // f16 [B,H,D] (may be q_new)
     void *K, *V;                        // cache: [B,S,H,D] or pages [num_pages,page_size,H,D]

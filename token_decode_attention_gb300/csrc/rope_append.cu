@@ -6,7 +6,8 @@
 //
 // For sequence b, head h and position p = current_pos[b]:
 //   theta_i = base^(-2 i / rope_dims) (fp64, on the host), a_i = p * theta_i
-//   (fp64: positions up to 2^31 would leave fp32 angles with no correct digits),
+//   reduced modulo 2 pi exactly in fixed point (positions up to 2^31 would
+//   leave an fp32 product p * theta_i with no correct digits),
 //   pairs (i, i + rope_dims/2), or (2i, 2i + 1) when `traditional`,
 //   (u, w) -> (u cos a - w sin a, u sin a + w cos a) in fp32, rounded to f16;
 //   channels from rope_dims on are copied.  q_out gets the rotated q; the cache
@@ -23,23 +24,19 @@
 namespace dattn {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 
-// 2*pi split for Cody-Waite reduction: kTwoPiHi is 2*pi rounded to double,
-// kTwoPiLo = 2*pi - kTwoPiHi.
-constexpr double kTwoPiHi = 6.283185307179586232;
-constexpr double kTwoPiLo = 2.4492935982947064e-16;
-constexpr double kInvTwoPi = 0.15915494309189533577;
-
-// cos/sin of p * theta: the product and its reduction to [-pi, pi] in fp64
-// (a few fp64 FMAs; p * theta reaches 2^31 radians), then fp32 sincosf of the
-// reduced angle, whose error (~3e-7 rad) is far below an f16 ulp.
-__device__ __forceinline__ void angle_sincos(uint32_t p, double theta, float *c, float *s) {
-    const double a = static_cast<double>(p) * theta;
-    const double k = rint(a * kInvTwoPi);
-    double r = fma(-k, kTwoPiHi, a);
-    r = fma(-k, kTwoPiLo, r);
-    sincosf(static_cast<float>(r), s, c);
+// cos/sin of p * theta_i from the turn fraction f_i = theta_i / (2 pi) held as
+// a 64-bit binary fraction.  p * f_i mod 1 is an exact wrapping integer
+// product (the angle reduced modulo 2 pi with no rounding, whatever the size
+// of p); its top 32 bits, as a signed fraction of a half turn, go to
+// sincospif.  Angle error: 2^-24 pi from the float conversion, ~1.5e-9 rad
+// from the dropped low bits.
+__device__ __forceinline__ void angle_sincos(uint32_t p, unsigned long long f, float *c,
+                                             float *s) {
+    const unsigned long long turns = static_cast<unsigned long long>(p) * f;  // mod 2^64
+    const int half_turns = static_cast<int>(static_cast<unsigned>(turns >> 32));
+    sincospif(static_cast<float>(half_turns) * 0x1p-31f, s, c);
 }
 
 template <int VP>  // pairs per work item: 4 when rope_dims % 8 == 0, else 1
@@ -130,7 +127,7 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(const RopeAppendA
     const uint32_t p = __ldg(a.cur_pos + b);
 
     for (int i = threadIdx.x; i < half; i += kThreads)
-        angle_sincos(p, a.theta[i], &cos_t[i], &sin_t[i]);
+        angle_sincos(p, a.turn_frac[i], &cos_t[i], &sin_t[i]);
 
     // first cache row (b, p, h0), or none when the position or its page is invalid
     long long row0 = -1;
