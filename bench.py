@@ -306,65 +306,87 @@ class Replica:
         return ms, clocks
 
     def e2e(self, steps: int, warmup: int, stream):
-        """Same metric through the public API with host buffers: each step copies
-        Q, the new token's K/V row and current_pos from pinned host memory,
-        rotates q and k at current_pos and appends k, v to the cache
-        (dattn_rope_append_f16), runs the decode and reads out back into pinned
-        host memory.  The KV cache itself is device-resident state."""
+        """Same metric through the public API with host buffers.  Each step copies
+        the new token's inputs (q, k, v rows and current_pos, packed in one pinned
+        host buffer) to the device in one copy, rotates q and k at current_pos and
+        appends k, v to the cache (dattn_rope_append_f16), runs the decode and
+        copies out back into pinned host memory.  The KV cache itself is
+        device-resident state."""
         if self.page_size:
             return None  # measured on the dense layout only
         w = self.w
         x = self.sets[0]
         B, H, D = w.batch, w.n_heads, w.head_dim
-        q_h = x["q"].cpu().pin_memory()
-        cp_h = x["cur_pos"].cpu().pin_memory()
+        n = B * H * D
+        # one pinned staging buffer: q | k_new | v_new (f16) | current_pos (u32)
+        pack_h = torch.empty((3 * n * 2 + 4 * B,), dtype=torch.uint8).pin_memory()
         last = np.minimum(self.cp_host.astype(np.int64), w.seq_len - 1)
-        knew_h = torch.stack([x["k"][b, int(last[b])] for b in range(B)]).cpu().pin_memory()
-        vnew_h = torch.stack([x["v"][b, int(last[b])] for b in range(B)]).cpu().pin_memory()
+        k_rows = torch.stack([x["k"][b, int(last[b])] for b in range(B)]).cpu()
+        v_rows = torch.stack([x["v"][b, int(last[b])] for b in range(B)]).cpu()
+        halves = pack_h[: 6 * n].view(torch.float16)
+        halves[:n].copy_(x["q"].cpu().reshape(-1))
+        halves[n:2 * n].copy_(k_rows.reshape(-1))
+        halves[2 * n:].copy_(v_rows.reshape(-1))
+        pack_h[6 * n:].view(torch.int32).copy_(x["cur_pos"].cpu())
+        pack_d = torch.empty(pack_h.shape, dtype=torch.uint8, device=self.device)
+        dh = pack_d[: 6 * n].view(torch.float16)
+        q_d, knew_d, vnew_d = (dh[i * n:(i + 1) * n].view(B, H, D) for i in range(3))
+        cp_d = pack_d[6 * n:].view(torch.int32)
         out_h = torch.empty((B, H, D), dtype=torch.float16).pin_memory()
-        q_d = torch.empty_like(x["q"])
-        cp_d = torch.empty_like(x["cur_pos"])
-        knew_d = torch.empty((B, H, D), dtype=torch.float16, device=self.device)
-        vnew_d = torch.empty_like(knew_d)
         out_d = self.outs[0]
-        h2d = (q_h.numel() + knew_h.numel() + vnew_h.numel()) * 2 + cp_h.numel() * 4
+        h2d = pack_h.numel()
         d2h = out_h.numel() * 2
 
         stream.wait_stream(torch.cuda.current_stream(self.device))
 
         def one():
-            q_d.copy_(q_h, non_blocking=True)
-            cp_d.copy_(cp_h, non_blocking=True)
-            knew_d.copy_(knew_h, non_blocking=True)
-            vnew_d.copy_(vnew_h, non_blocking=True)
+            pack_d.copy_(pack_h, non_blocking=True)
             self.dattn.dattn_rope_append_f16(q_d, knew_d, vnew_d, q_d, x["k"], x["v"], cp_d,
                                              stream=stream)
             self.dattn.dattn_decode_f16_ex(q_d, x["k"], x["v"], out_d, cp_d, self.ws,
                                            self.partitions, stream)
             out_h.copy_(out_d, non_blocking=True)
 
-        with torch.cuda.stream(stream):
-            for _ in range(warmup):
-                one()
-            torch.cuda.synchronize()
+        def timed(step):
             start = torch.cuda.Event(enable_timing=True)
             end = torch.cuda.Event(enable_timing=True)
             t0 = time.perf_counter()
             start.record(stream)
             for _ in range(steps):
-                one()
+                step()
             end.record(stream)
             torch.cuda.synchronize()
-            wall = time.perf_counter() - t0
-        ms = start.elapsed_time(end) / steps
+            return start.elapsed_time(end) / steps, (time.perf_counter() - t0) * 1e3 / steps
+
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                one()
+            torch.cuda.synchronize()
+            eager_ms, eager_wall = timed(one)
+            # the same step recorded once with the library's batch API (outside the
+            # timed region) and submitted as one batch per step
+            self.dattn.dattn_batch_begin(stream)
+            one()
+            batch = self.dattn.dattn_batch_end(stream)
+            for _ in range(warmup):
+                batch.launch(stream)
+            torch.cuda.synchronize()
+            ms, wall = timed(lambda: batch.launch(stream))
+            nodes = batch.nodes
+            batch.close()
         return {"value": self.bytes_per_step / (ms * 1e-3) / 1e9, "unit": "GB/s",
-                "ms_per_step": ms, "wall_ms_per_step": wall * 1e3 / steps,
+                "ms_per_step": ms, "wall_ms_per_step": wall,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "launches_per_step": 1 + self.launches_per_step,
-                "note": "Q, new K/V row and current_pos copied H2D from pinned memory, "
-                        "q and k rotated and K/V row appended at current_pos "
-                        "(dattn_rope_append_f16), decode, out copied D2H; the KV cache is "
-                        "device-resident state; value counts the decode's bytes only"}
+                "submission": f"one dattn_batch_launch per step ({nodes} recorded operations)",
+                "eager": {"value": self.bytes_per_step / (eager_ms * 1e-3) / 1e9,
+                          "ms_per_step": eager_ms, "wall_ms_per_step": eager_wall},
+                "note": "one H2D copy of the new token's q, k, v rows and current_pos from "
+                        "pinned memory, q and k rotated and the K/V row appended at "
+                        "current_pos (dattn_rope_append_f16), decode, out copied D2H into "
+                        "pinned memory; 'eager' issues the same calls from Python each step; "
+                        "the KV cache is device-resident state; value counts the decode's "
+                        "bytes only"}
 
 
 def graph_time_us(fn, steps: int, warmup: int, stream) -> float:

@@ -298,8 +298,11 @@ int dattn_softmax_f32(const float *x, float *out, long long rows, int cols,
  *
  * Calls that may be recorded: dattn_decode_f16_ex, dattn_decode_paged_f16,
  * dattn_decode_f16_noalloc after its first call on the device, dattn_qk_f16,
- * dattn_pv_f16, and dattn_decode_f16 once its workspace is large enough (a
- * recorded call must not allocate).  The shape's plan is made when a call is
+ * dattn_pv_f16, dattn_rope_append_f16, dattn_rope_append_paged_f16,
+ * dattn_softmax_f32, and dattn_decode_f16 once its workspace is large enough
+ * (a recorded call must not allocate).  Copies the caller issues on the same
+ * stream meanwhile (cudaMemcpyAsync from pinned host memory, for example) are
+ * recorded too.  The shape's plan is made when a call is
  * recorded; make one ordinary call per shape first if its set-up should not
  * happen during recording.  `stream` must be a created stream, not NULL.
  * Errors: INVALID_ARG, CUDA (for example a recorded call that synchronised).

@@ -592,14 +592,28 @@ int rope_append(const void *q_new, const void *k_new, const void *v_new, void *q
     a.S = seq_len;
     a.rope_dims = rope_dims;
     a.traditional = traditional ? 1 : 0;
-    // theta_i < 1 < 2 pi, so theta_i / (2 pi) is a fraction of a turn below 1/6;
-    // scaled by 2^64 in extended precision it fits in 63 bits.
-    const long double two_pi = 6.283185307179586476925286766559005768L;
-    for (int i = 0; i < rope_dims / 2; ++i) {
-        const double theta = std::pow(rope_base, -2.0 * i / rope_dims);
-        a.turn_frac[i] = static_cast<unsigned long long>(
-            std::llroundl(std::ldexp(static_cast<long double>(theta) / two_pi, 64)));
+    // The table depends on (rope_dims, rope_base) only; a decode loop passes the
+    // same pair every step, so the last one is kept per thread (long double is
+    // software arithmetic on some hosts).
+    struct TurnTable {
+        int rope_dims = 0;
+        double base = 0.0;
+        unsigned long long frac[dattn::kRopeMaxPairs];
+    };
+    thread_local TurnTable table;
+    if (table.rope_dims != rope_dims || table.base != rope_base) {
+        // theta_i <= 1 < 2 pi, so theta_i / (2 pi) is a fraction of a turn below
+        // 1/6; scaled by 2^64 in extended precision it fits in 63 bits.
+        const long double two_pi = 6.283185307179586476925286766559005768L;
+        for (int i = 0; i < rope_dims / 2; ++i) {
+            const double theta = std::pow(rope_base, -2.0 * i / rope_dims);
+            table.frac[i] = static_cast<unsigned long long>(
+                std::llroundl(std::ldexp(static_cast<long double>(theta) / two_pi, 64)));
+        }
+        table.rope_dims = rope_dims;
+        table.base = rope_base;
     }
+    std::memcpy(a.turn_frac, table.frac, sizeof(unsigned long long) * (rope_dims / 2));
     // about four CTAs per SM of work, at most 8 heads per CTA
     const long long bh = static_cast<long long>(batch) * n_heads;
     a.heads_per_cta = static_cast<int>(
