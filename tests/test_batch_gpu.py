@@ -105,3 +105,44 @@ def test_growing_the_library_workspace_while_recording_is_refused_cleanly():
     torch.cuda.synchronize()
     ref = oracle.decode_f64(to_np(q), to_np(k), to_np(v), np.array([4999], np.uint32))
     assert_decode_close(out, ref, "after the refused recording")
+
+
+def test_recorded_decode_step_advances_one_token_per_replay():
+    # one recorded step -- rotate and append the new token, then attend -- replayed
+    # for three consecutive tokens with new q, k, v and current_pos written into
+    # the same buffers between replays
+    g = torch.Generator(device="cuda").manual_seed(321)
+    B, H, D, S = 2, 16, 128, 64
+    K, V = rand_f16(g, (B, S, H, D)), rand_f16(g, (B, S, H, D))
+    K_host, V_host = to_np(K).copy(), to_np(V).copy()
+    q, kn, vn = (torch.empty((B, H, D), dtype=torch.float16, device="cuda") for _ in range(3))
+    cp = torch.empty((B,), dtype=torch.int32, device="cuda")
+    q_rot, out = torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(max(16, dattn.dattn_decode_workspace_bytes(B, H, D, S)), dtype=torch.uint8,
+                     device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    dattn.dattn_batch_begin(s)
+    try:
+        dattn.dattn_rope_append_f16(q, kn, vn, q_rot, K, V, cp, stream=s)
+        dattn.dattn_decode_f16_ex(q_rot, K, V, out, cp, ws, 0, s)
+    finally:
+        batch = dattn.dattn_batch_end(s)
+    try:
+        for step, pos in enumerate(([40, 10], [41, 11], [42, 12])):
+            _fill(g, q, kn, vn)
+            cp.copy_(cur_pos_tensor(pos))
+            torch.cuda.synchronize()
+            batch.launch(s)
+            s.synchronize()
+            q_ref = oracle.rope_f64(to_np(q), pos).astype(np.float16)
+            k_ref = oracle.rope_f64(to_np(kn), pos).astype(np.float16)
+            for b in range(B):
+                K_host[b, pos[b]] = k_ref[b]
+                V_host[b, pos[b]] = to_np(vn[b])
+            ref = oracle.decode_f64(q_ref, K_host, V_host, np.asarray(pos, np.uint32))
+            assert_decode_close(out, ref, f"recorded step {step}")
+    finally:
+        batch.close()
+    assert dattn.dattn_device_error(clear=True) == _native.OK
