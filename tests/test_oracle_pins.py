@@ -447,6 +447,13 @@ def test_softmax_closed_forms_and_invariants():
     d = float(y[0, 0]) - float(y[0, 1])
     np.testing.assert_allclose(oracle.softmax_f64(y)[0],
                                [1 / (1 + math.exp(-d)), 1 / (1 + math.exp(d))], rtol=1e-15)
+    # -inf entries get weight exactly 0; a row far above the rest is one-hot
+    w = np.array([[0.5, -np.inf, 1.0, -np.inf], [1000.0, 0.0, -3.0, 2.0]], np.float32)
+    ow = oracle.softmax_f64(w)
+    assert ow[0, 1] == 0.0 and ow[0, 3] == 0.0
+    np.testing.assert_allclose(ow[0, [0, 2]], [1 / (1 + math.exp(0.5)), 1 / (1 + math.exp(-0.5))],
+                               rtol=1e-15)
+    assert np.array_equal(ow[1], [1.0, 0.0, 0.0, 0.0])
     # all -inf or a NaN gives NaN for that row only
     z = rng.standard_normal((3, 4)).astype(np.float32)
     z[0] = -np.inf
@@ -461,7 +468,9 @@ def _rope_complex(x64, pos, rd, base, traditional):
     # the same rotation as complex multiplication by exp(i a), with numpy
     B, H, D = x64.shape
     half = rd // 2
-    theta = base ** (-2.0 * np.arange(half) / rd)
+    # theta_i from C's pow (math.pow), not numpy's vectorised power: at positions
+    # near 2^31 a one-ulp difference in theta moves the angle by ~2e-7 rad
+    theta = np.array([math.pow(base, -2.0 * i / rd) for i in range(half)])
     a = np.asarray(pos, np.float64)[:, None, None] * theta[None, None, :]
     if traditional:
         z = x64[..., 0:rd:2] + 1j * x64[..., 1:rd:2]
@@ -480,8 +489,8 @@ def _rope_complex(x64, pos, rd, base, traditional):
 @pytest.mark.parametrize("rd", [8, 64, 128])
 def test_rope_equals_complex_rotation(traditional, rd):
     rng = np.random.default_rng(60 + rd)
-    x = rand_f16(rng, (3, 4, 128))
-    pos = np.array([0, 17, 131071], np.uint32)
+    x = rand_f16(rng, (4, 4, 128))
+    pos = np.array([0, 17, 131071, 2**31 - 1], np.uint32)
     got = oracle.rope_f64(x, pos, rd, 10000.0, traditional)
     ref = _rope_complex(x.astype(np.float64), pos, rd, 10000.0, traditional)
     np.testing.assert_allclose(got, ref, rtol=1e-9, atol=1e-9)
