@@ -389,30 +389,42 @@ class Replica:
                         "bytes only"}
 
 
-def graph_time_us(fn, steps: int, warmup: int, stream) -> float:
+def graph_time_us(fn, steps: int, warmup: int, stream, graph: bool = True) -> float:
     """Device time per call of `fn(i, stream)`: `steps` calls captured in one
-    CUDA graph, replayed once between two events on `stream`."""
+    CUDA graph, replayed once between two events on `stream` (or, with
+    graph=False, issued eagerly between the events)."""
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
         for i in range(warmup):
             fn(i, stream)
         torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(steps):
-                fn(i, stream)
-        g.replay()
-        torch.cuda.synchronize()
+        g = None
+        if graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(steps):
+                    fn(i, stream)
+            g.replay()
+            torch.cuda.synchronize()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record(stream)
-        g.replay()
+        if g is not None:
+            g.replay()
+        else:
+            for i in range(steps):
+                fn(i, stream)
         end.record(stream)
         torch.cuda.synchronize()
     return start.elapsed_time(end) * 1e3 / steps
 
 
-def sweep_ops(device, stream, steps: int, warmup: int, peak: float) -> dict:
+OPS = ["rope_append_7b", "rope_append_ragged", "rope_append_outlier", "softmax_10240x8192",
+       "softmax_65536x1024"]
+
+
+def sweep_ops(device, stream, steps: int, warmup: int, peak: float, only: str | None = None,
+              graph: bool = True) -> dict:
     """The two other kernels of a decode step, each timed alone.
 
     rope_append: rotate the new q and k and append k, v at current_pos, for the
@@ -424,6 +436,8 @@ def sweep_ops(device, stream, steps: int, warmup: int, peak: float) -> dict:
     import token_decode_attention_gb300 as dattn
     res = {}
     for name in ("7b", "ragged", "outlier"):
+        if only is not None and only != f"rope_append_{name}":
+            continue
         w = WORKLOADS[name]
         B, H, D, S = w.batch, w.n_heads, w.head_dim, w.seq_len
         try:
@@ -439,7 +453,7 @@ def sweep_ops(device, stream, steps: int, warmup: int, peak: float) -> dict:
                 (draw_current_pos(w) % cache_s).astype(np.int64)).to(torch.int32).to(device)
             torch.cuda.synchronize()
             us = graph_time_us(lambda i, st: dattn.dattn_rope_append_f16(
-                new[0], new[1], new[2], qo, K, V, cp, stream=st), steps, warmup, stream)
+                new[0], new[1], new[2], qo, K, V, cp, stream=st), steps, warmup, stream, graph)
             nbytes = 6 * B * H * D * 2 + 4 * B
             res[f"rope_append_{name}"] = {"us_per_call": us, "GB/s": nbytes / us / 1e3,
                                           "algorithmic_bytes": nbytes,
@@ -451,6 +465,8 @@ def sweep_ops(device, stream, steps: int, warmup: int, peak: float) -> dict:
             res[f"rope_append_{name}"] = {"error": f"{type(e).__name__}: {e}"}
     for rows, cols in ((10240, 8192), (65536, 1024)):
         key = f"softmax_{rows}x{cols}"
+        if only is not None and only != key:
+            continue
         try:
             g = torch.Generator(device=device).manual_seed(rows + cols)
             xs = [torch.empty((rows, cols), dtype=torch.float32, device=device).normal_(
@@ -458,7 +474,7 @@ def sweep_ops(device, stream, steps: int, warmup: int, peak: float) -> dict:
             ys = [torch.empty_like(x) for x in xs]
             torch.cuda.synchronize()
             us = graph_time_us(lambda i, st: dattn.dattn_softmax_f32(xs[i % 2], ys[i % 2], st),
-                               steps, warmup, stream)
+                               steps, warmup, stream, graph)
             nbytes = 8 * rows * cols
             gbs = nbytes / us / 1e3
             res[key] = {"us_per_call": us, "GB/s": gbs, "frac_of_measured": gbs / peak,
@@ -575,6 +591,8 @@ def main():
     ap.add_argument("--profile", action="store_true",
                     help="only warm-up and timed steps of one workload (for ncu captures)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--op", default="", choices=[""] + OPS,
+                    help="with --profile: time this other kernel of the decode step instead")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_env()
@@ -601,6 +619,13 @@ def main():
     peak, peak_kind = hbm_peak()
     stream = torch.cuda.Stream(device=device)
 
+    if args.profile and args.op:
+        r = sweep_ops(device, stream, args.steps, args.warmup, peak, only=args.op,
+                      graph=not args.eager)
+        print(json.dumps({"profile": args.op, **r[args.op]}), flush=True)
+        if "error" in r[args.op]:
+            raise SystemExit(1)
+        return
     rep = Replica(args.workload, device, l2, args.partitions,
                   args.batch if args.profile else 0, args.paged)
     sampler = ClockSampler(local)

@@ -31,8 +31,13 @@ def check(x: torch.Tensor, out: torch.Tensor):
     assert (err <= ATOL + RTOL * np.abs(ref[~nan])).all(), f"max err {err.max():.3g}"
 
 
+# widths cover: one warp per row (<= 1024); one CTA per row held in registers
+# (<= 8192) as float4 slots (cols % 4 == 0: 2, 4, 8 per thread) or scalar slots
+# (8, 16, 32 per thread); two passes beyond 8192
 @pytest.mark.parametrize("rows,cols", [(1, 1), (7, 5), (64, 32), (33, 1000), (5, 1024),
-                                       (9, 1025), (4, 4096), (3, 8191), (2, 131072)])
+                                       (9, 1025), (6, 2052), (4, 4096), (2, 6000), (3, 8192),
+                                       (5, 3001), (3, 8191), (2, 8193), (2, 8196),
+                                       (2, 131072)])
 def test_softmax_matches_oracle(rows, cols):
     g = torch.Generator(device="cuda").manual_seed(rows * 100003 + cols)
     x = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
@@ -44,7 +49,7 @@ def test_softmax_matches_oracle(rows, cols):
 
 def test_softmax_masked_and_degenerate_rows():
     g = torch.Generator(device="cuda").manual_seed(3)
-    for cols in (300, 5000):  # one warp per row, one CTA per row
+    for cols in (300, 5000, 5001, 9000):  # warp per row; CTA per row: float4, scalar, 2 passes
         x = torch.empty((6, cols), dtype=torch.float32, device="cuda")
         x.normal_(0.0, 3.0, generator=g)
         x[0, ::3] = float("-inf")          # masked entries: weight 0

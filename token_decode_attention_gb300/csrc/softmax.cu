@@ -4,11 +4,14 @@
 //   out[r, c] = exp(x[r, c] - max_c x[r, c]) / sum_c exp(x[r, c] - max_c x[r, c]).
 // It is the max-subtracted softmax of the decode path (running max, sum of
 // exponentials) exposed on its own.  HBM-bound: 8 bytes per element when a row
-// fits in registers, 12 when it is read twice.
+// stays on chip, 12 when it is read twice.
 //
 //   short rows (cols <= 1024): one warp per row, the row kept in registers
 //     (32 values per lane), warp-shuffle max and sum: one read, one write;
-//   long rows: one CTA per row, a pass computing the running (max, sum) per
+//   rows up to 8192: one CTA of 256 threads per row, the row kept in
+//     registers (up to 32 values per thread), block max and sum through
+//     shared memory: one read, one write;
+//   longer rows: one CTA per row, a pass computing the running (max, sum) per
 //     thread merged across the block, then a pass writing the output.
 #include <cuda_runtime.h>
 
@@ -62,6 +65,82 @@ __global__ void __launch_bounds__(256) softmax_warp_rows(const float *__restrict
     for (int i = 0; i < kPerLane; ++i) {
         const int c = lane + 32 * i;
         if (c < cols) orow[c] = v[i] * inv;
+    }
+}
+
+constexpr int kRegRowMax = 32 * kRowThreads;  // columns a CTA holds in registers
+
+// max (IS_MAX) or sum of one value per thread over the CTA; every thread gets it
+template <bool IS_MAX>
+__device__ __forceinline__ float block_all_reduce(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float u = __shfl_xor_sync(0xffffffffu, v, o);
+        v = IS_MAX ? fmaxf(v, u) : v + u;
+    }
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    v = red[0];
+#pragma unroll
+    for (int w = 1; w < kRowThreads / 32; ++w) v = IS_MAX ? fmaxf(v, red[w]) : v + red[w];
+    return v;
+}
+
+// One CTA per row, the row in registers: NV slots per thread, a slot being a
+// float4 (VEC, cols % 4 == 0) or a float.  Slot k of thread t covers element
+// (or float4) t + k * kRowThreads, so each load instruction is coalesced.
+// Padding is -infinity, which exponentiates to 0.  A NaN anywhere, or a row
+// of -infinity only (max - max = NaN), propagates through the sum to the
+// whole row, as the definition does.
+template <int NV, bool VEC>
+__global__ void __launch_bounds__(kRowThreads) softmax_reg_rows(const float *__restrict__ x,
+                                                                float *__restrict__ out,
+                                                                int cols) {
+    __shared__ float red_m[kRowThreads / 32], red_l[kRowThreads / 32];
+    constexpr int W = VEC ? 4 : 1;
+    const long long r = blockIdx.x;
+    const int n = VEC ? cols / 4 : cols;
+    float v[NV][W];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int c = threadIdx.x + k * kRowThreads;
+        if constexpr (VEC) {
+            float4 t = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (c < n) t = __ldcs(reinterpret_cast<const float4 *>(x + r * cols) + c);
+            v[k][0] = t.x;
+            v[k][1] = t.y;
+            v[k][2] = t.z;
+            v[k][3] = t.w;
+        } else {
+            v[k][0] = c < n ? __ldcs(x + r * cols + c) : -INFINITY;
+        }
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+#pragma unroll
+        for (int e = 0; e < W; ++e) m = fmaxf(m, v[k][e]);
+    m = block_all_reduce<true>(m, red_m);
+    float l = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+#pragma unroll
+        for (int e = 0; e < W; ++e) {
+            v[k][e] = expf(v[k][e] - m);
+            l += v[k][e];
+        }
+    l = block_all_reduce<false>(l, red_l);
+    const float inv = 1.f / l;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int c = threadIdx.x + k * kRowThreads;
+        if (c < n) {
+            if constexpr (VEC)
+                __stcs(reinterpret_cast<float4 *>(out + r * cols) + c,
+                       make_float4(v[k][0] * inv, v[k][1] * inv, v[k][2] * inv, v[k][3] * inv));
+            else
+                __stcs(out + r * cols + c, v[k][0] * inv);
+        }
     }
 }
 
@@ -153,6 +232,23 @@ cudaError_t launch_softmax(const float *x, float *out, long long rows, int cols,
     if (rows > 0x7fffffffLL) return cudaErrorInvalidValue;
     bool vec4 = (cols % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
                 ((reinterpret_cast<uintptr_t>(out) & 15u) == 0);
+    if (cols <= kRegRowMax) {
+        // smallest register footprint that holds the row
+        const int per_thread = (cols + kRowThreads - 1) / kRowThreads;  // 5 .. 32 floats
+        const void *fn;
+        if (vec4) {
+            fn = per_thread <= 8    ? reinterpret_cast<const void *>(softmax_reg_rows<2, true>)
+                 : per_thread <= 16 ? reinterpret_cast<const void *>(softmax_reg_rows<4, true>)
+                                    : reinterpret_cast<const void *>(softmax_reg_rows<8, true>);
+        } else {
+            fn = per_thread <= 8    ? reinterpret_cast<const void *>(softmax_reg_rows<8, false>)
+                 : per_thread <= 16 ? reinterpret_cast<const void *>(softmax_reg_rows<16, false>)
+                                    : reinterpret_cast<const void *>(softmax_reg_rows<32, false>);
+        }
+        void *args[] = {&x, &out, &cols};
+        return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(rows)), dim3(kRowThreads), args, 0,
+                                stream);
+    }
     void *args[] = {&x, &out, &cols, &vec4};
     return cudaLaunchKernel(reinterpret_cast<const void *>(softmax_block_rows),
                             dim3(static_cast<unsigned>(rows)), dim3(kRowThreads), args, 0, stream);
