@@ -8,7 +8,8 @@ rotation and the position invariants in tests/test_oracle_pins.py.
 
 Bound, per element: one f16 ulp of the fp64 value (the single rounding to
 f16) plus 1e-6 (|u| + |w|) for the element's pair (u, w).  The kernel reduces
-p * theta modulo 2 pi in fp64 and takes fp32 cos/sin of the reduced angle
+p * theta modulo 2 pi exactly, as a wrapping integer product with theta / 2 pi
+held as a 64-bit binary fraction, and takes fp32 cos/sin of the reduced angle
 (angle error below 4e-7 rad), then rotates in fp32 (about 2e-7 relative to
 |u| + |w|).  Channels past rope_dims are copied, so their bound is zero.
 """

@@ -113,6 +113,10 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
     }
 
     pdl_wait_primary();  // the decode kernel's workspace writes are visible after this
+    // the next kernel on the stream may start its launch now; one launched with
+    // programmatic dependent launch waits for this grid to complete before it
+    // reads anything
+    pdl_launch_dependents();
     if (a.B > kInlinePrefix) {
         before = a.ws_prefix[b];
         total = a.ws_prefix[a.B];
@@ -158,22 +162,34 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
     sm_l[tid] = L;
     sm_a[tid] = A;
     __syncthreads();
-    // tree fold over the pieces-in-flight index, for each float4 lane
-    for (int step = 1; step < nsub; step <<= 1) {
-        if (sub < nsub && (sub % (2 * step)) == 0 && sub + step < nsub) {
-            const int t = tid, o = tid + step * f4;
-            float m2 = sm_m[t], l2 = sm_l[t];
-            float4 a2 = sm_a[t];
+    // Two-level fold over the pieces-in-flight index, for each float4 lane:
+    // groups of eight subs, then the (at most eight) group results.  Each
+    // level-1 thread reads only its own group and writes the group's first
+    // entry, so the level needs no barrier inside it.
+    const int ngroups = (nsub + 7) / 8;
+    if (tid < ngroups * f4) {
+        const int q = tid / f4, fq = tid - q * f4;
+        const int s_end = min(nsub, q * 8 + 8);
+        const int t0 = q * 8 * f4 + fq;
+        float m2 = sm_m[t0], l2 = sm_l[t0];
+        float4 a2 = sm_a[t0];
+        for (int s2 = q * 8 + 1; s2 < s_end; ++s2) {
+            const int o = s2 * f4 + fq;
             fold(m2, l2, a2, sm_m[o], sm_l[o], sm_a[o]);
-            sm_m[t] = m2;
-            sm_l[t] = l2;
-            sm_a[t] = a2;
         }
-        __syncthreads();
+        sm_m[t0] = m2;
+        sm_l[t0] = l2;
+        sm_a[t0] = a2;
     }
+    __syncthreads();
     if (tid < f4) {
-        const float4 A2 = sm_a[tid];
-        const float inv = 1.f / sm_l[tid];
+        float m2 = sm_m[tid], l2 = sm_l[tid];
+        float4 A2 = sm_a[tid];
+        for (int q = 1; q < ngroups; ++q) {
+            const int o = q * 8 * f4 + tid;
+            fold(m2, l2, A2, sm_m[o], sm_l[o], sm_a[o]);
+        }
+        const float inv = 1.f / l2;
         __half2 lo = __floats2half2_rn(A2.x * inv, A2.y * inv);
         __half2 hi = __floats2half2_rn(A2.z * inv, A2.w * inv);
         uint2 packed;

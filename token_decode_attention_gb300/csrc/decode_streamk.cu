@@ -167,6 +167,20 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     uint64_t *empty_bar = full_bar + a.stages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty_bar + a.stages);
 
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.stages; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], a.active_warps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    // Launched with programmatic dependent launch: up to here only shared memory
+    // is touched, so this CTA may already be resident while the kernel before it
+    // on the stream finishes.  Everything after the wait sees that kernel's writes
+    // (current_pos, Q, the cache).
+    pdl_wait_primary();
+
     // ---- the CTA's range: block scan of the live lengths over the batch ----
     const long long per = (a.B + kThreads - 1) / kThreads;
     const long long bb = min(static_cast<long long>(threadIdx.x) * per, static_cast<long long>(a.B));
@@ -180,14 +194,6 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         if (lane >= o) incl += y;
     }
     if (lane == 31) s_warp_sum[warp] = incl;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < a.stages; ++i) {
-            mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], a.active_warps);
-        }
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
     __syncthreads();
     long long before = 0, total = 0;
 #pragma unroll
@@ -612,8 +618,18 @@ cudaError_t launch_decode(const DecodeArgs &a, DecodeVariant v, int smem, cudaSt
     const void *fn = variant_fn(v);
     if (fn == nullptr || a.partitions <= 0) return cudaErrorInvalidValue;
     void *args[] = {const_cast<DecodeArgs *>(&a)};
-    return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(a.partitions)),
-                            dim3(decode_threads(v.nwc)), args, static_cast<size_t>(smem), stream);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.partitions));
+    cfg.blockDim = dim3(decode_threads(v.nwc));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    // the kernel waits (griddepcontrol.wait) before its first global-memory access
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 cudaError_t decode_occupancy(DecodeVariant v, int smem, int *ctas_per_sm) {
