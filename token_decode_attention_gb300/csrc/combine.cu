@@ -13,10 +13,9 @@
 // Grid: one CTA per (sequence, head, chunk of channels).  The host picks the
 // chunk width from the expected number of pieces per unit: whole heads when
 // units have few pieces (many sequences), narrow chunks when one sequence is
-// spread over every partition, so each thread folds only a few pieces.  Each
-// thread folds its pieces online (running max, rescaled sum and accumulator)
-// after issuing their loads together; the per-thread states are folded once
-// more through shared memory.  Launched with
+// spread over every partition, so each thread folds only a few pieces (the
+// merge itself is merge::merge_task, shared with the decode kernel's fused
+// merge).  Launched with
 // programmatic dependent launch: it may start while the decode kernel drains
 // and waits on griddepcontrol.wait before touching the workspace.
 #include <cuda_fp16.h>
@@ -26,6 +25,7 @@
 
 #include "dattn_internal.h"
 #include "ptx.cuh"
+#include "merge.cuh"
 #include "streamk.h"
 
 namespace dattn {
@@ -33,38 +33,6 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kInlinePrefix = 4096;  // batches summed from current_pos in the combine
-
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// Fold one state (m, l, acc) into a running state, rescaling whichever of the
-// two has the smaller maximum.
-__device__ __forceinline__ void fold(float &M, float &L, float4 &A, float m, float l, float4 a) {
-    if (l <= 0.f) return;
-    if (m > M) {
-        const float s = fast_exp2(M - m);  // 0 when M is -inf
-        L *= s;
-        A.x *= s;
-        A.y *= s;
-        A.z *= s;
-        A.w *= s;
-        M = m;
-    }
-    const float w = fast_exp2(m - M);
-    L = fmaf(w, l, L);
-    A.x = fmaf(w, a.x, A.x);
-    A.y = fmaf(w, a.y, A.y);
-    A.z = fmaf(w, a.z, A.z);
-    A.w = fmaf(w, a.w, A.w);
-}
-
-__device__ __forceinline__ long long live_len(const uint32_t *cp, long long b, int S) {
-    const uint32_t c = __ldg(cp + b);
-    return c >= static_cast<uint32_t>(S - 1) ? S : static_cast<long long>(c) + 1;
-}
 
 __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) {
     __shared__ float sm_m[kThreads], sm_l[kThreads];
@@ -82,7 +50,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
     const long long u = b * a.head_groups + g;
 
     const int tid = threadIdx.x;
-    const long long Lb = live_len(a.cur_pos, b, a.S);
+    const long long Lb = merge::live_len(a.cur_pos, b, a.S);
     // Live positions before sequence b and in total.  For batches of up to
     // kInlinePrefix sequences they are summed here from current_pos (an input,
     // readable before the decode kernel finishes); larger batches read the
@@ -90,7 +58,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
     long long before = 0, total = 0;
     if (a.B <= kInlinePrefix) {
         for (int i = tid; i < a.B; i += kThreads) {
-            const long long L = live_len(a.cur_pos, i, a.S);
+            const long long L = merge::live_len(a.cur_pos, i, a.S);
             total += L;
             if (i < b) before += L;
         }
@@ -131,73 +99,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
 
     const int c0 = chunk * a.chunk;
     const int width = min(a.chunk, a.D - c0);  // a multiple of 8
-    const int f4 = width / 4;                  // float4 per piece row
-    const int nsub = kThreads / f4;            // pieces in flight
-    const int sub = tid / f4, f = tid - sub * f4;
-    const size_t hgs = a.heads_per_cta;
-
-    float M = -INFINITY, L = 0.f;
-    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (sub < nsub) {
-        // issue the loads of up to eight pieces before folding any of them
-        for (int j0 = sub; j0 < npieces; j0 += 8 * nsub) {
-            float2 ml[8];
-            float4 v[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int j = j0 + r * nsub;
-                ml[r] = make_float2(-INFINITY, 0.f);
-                v[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (j < npieces) {
-                    const size_t row = static_cast<size_t>(piece_slot(c_first + j, u)) * hgs + hl;
-                    ml[r] = a.ws_ml[row];
-                    v[r] = *reinterpret_cast<const float4 *>(a.ws_acc + row * a.D + c0 + f * 4);
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 8; ++r) fold(M, L, A, ml[r].x, ml[r].y, v[r]);
-        }
-    }
-    sm_m[tid] = M;
-    sm_l[tid] = L;
-    sm_a[tid] = A;
-    __syncthreads();
-    // Two-level fold over the pieces-in-flight index, for each float4 lane:
-    // groups of eight subs, then the (at most eight) group results.  Each
-    // level-1 thread reads only its own group and writes the group's first
-    // entry, so the level needs no barrier inside it.
-    const int ngroups = (nsub + 7) / 8;
-    if (tid < ngroups * f4) {
-        const int q = tid / f4, fq = tid - q * f4;
-        const int s_end = min(nsub, q * 8 + 8);
-        const int t0 = q * 8 * f4 + fq;
-        float m2 = sm_m[t0], l2 = sm_l[t0];
-        float4 a2 = sm_a[t0];
-        for (int s2 = q * 8 + 1; s2 < s_end; ++s2) {
-            const int o = s2 * f4 + fq;
-            fold(m2, l2, a2, sm_m[o], sm_l[o], sm_a[o]);
-        }
-        sm_m[t0] = m2;
-        sm_l[t0] = l2;
-        sm_a[t0] = a2;
-    }
-    __syncthreads();
-    if (tid < f4) {
-        float m2 = sm_m[tid], l2 = sm_l[tid];
-        float4 A2 = sm_a[tid];
-        for (int q = 1; q < ngroups; ++q) {
-            const int o = q * 8 * f4 + tid;
-            fold(m2, l2, A2, sm_m[o], sm_l[o], sm_a[o]);
-        }
-        const float inv = 1.f / l2;
-        __half2 lo = __floats2half2_rn(A2.x * inv, A2.y * inv);
-        __half2 hi = __floats2half2_rn(A2.z * inv, A2.w * inv);
-        uint2 packed;
-        packed.x = *reinterpret_cast<uint32_t *>(&lo);
-        packed.y = *reinterpret_cast<uint32_t *>(&hi);
-        *reinterpret_cast<uint2 *>(reinterpret_cast<__half *>(a.out) + bh * a.D + c0 + tid * 4) =
-            packed;
-    }
+    merge::merge_task<kThreads>(a.ws_acc, a.ws_ml, a.out, a.D, a.heads_per_cta, bh, c0, width, u,
+                                hl, c_first, npieces, tid, sm_m, sm_l, sm_a,
+                                [] { __syncthreads(); });
 }
 
 }  // namespace

@@ -48,6 +48,9 @@ constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
 #ifndef DATTN_DEEP_RING_POSITIONS
 #define DATTN_DEEP_RING_POSITIONS (1LL << 40)
 #endif
+#ifndef DATTN_MIN_HEAD_GROUPS
+#define DATTN_MIN_HEAD_GROUPS 1  // split the heads into at least this many groups
+#endif
 #ifndef DATTN_MIN_POSITIONS
 #define DATTN_MIN_POSITIONS 16
 #endif
@@ -210,8 +213,9 @@ int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
     if (H > nwc * (32 / bdx) * kcap) nwc = 16;
     const int nlg = nwc * (32 / bdx);  // lane groups per CTA
     const int hg_max = std::min(nlg * kcap, std::max(1, kMaxRowBytesKV / (D * 4)));
-    p.NHG = (H + hg_max - 1) / hg_max;
+    p.NHG = std::max((H + hg_max - 1) / hg_max, std::min(H, DATTN_MIN_HEAD_GROUPS));
     p.HG = (H + p.NHG - 1) / p.NHG;
+    p.NHG = (H + p.HG - 1) / p.HG;  // no empty group
     p.PHI = p.HG >= nlg ? 1 : std::min(32, nlg / p.HG);
     const int kmax = (p.HG * p.PHI + nlg - 1) / nlg;
     p.v = DecodeVariant{bdx, ch, kmax, nwc};

@@ -1,0 +1,137 @@
+// merge.cuh -- log-sum-exp merge of the pieces of one (sequence, head, chunk
+// of channels), shared by the combine kernel and the decode kernel's fused
+// merge.
+//
+// Piece j of a unit left, per head, m_j = max score (log2 units),
+// l_j = sum 2^(s - m_j) and acc_j = sum 2^(s - m_j) V in workspace slot
+// piece_slot(c_first + j, u).  The exact softmax-weighted sum over the unit's
+// whole live range is
+//   out = sum_j 2^(m_j - M) acc_j / sum_j 2^(m_j - M) l_j,   M = max_j m_j.
+// NT threads share one task: thread (sub, f) folds pieces sub, sub + nsub, ...
+// of float4 column f online, after issuing the loads of up to eight of them
+// together; the per-thread states are then folded in two levels through shared
+// memory (groups of eight subs, then the group results).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "streamk.h"
+
+namespace dattn {
+namespace merge {
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Fold one state (m, l, acc) into a running state, rescaling whichever of the
+// two has the smaller maximum.  Empty states (l <= 0) change nothing.
+__device__ __forceinline__ void fold(float &M, float &L, float4 &A, float m, float l, float4 a) {
+    if (l <= 0.f) return;
+    if (m > M) {
+        const float s = ex2(M - m);  // 0 when M is -inf
+        L *= s;
+        A.x *= s;
+        A.y *= s;
+        A.z *= s;
+        A.w *= s;
+        M = m;
+    }
+    const float w = ex2(m - M);
+    L = fmaf(w, l, L);
+    A.x = fmaf(w, a.x, A.x);
+    A.y = fmaf(w, a.y, A.y);
+    A.z = fmaf(w, a.z, A.z);
+    A.w = fmaf(w, a.w, A.w);
+}
+
+__device__ __forceinline__ long long live_len(const uint32_t *cp, long long b, int S) {
+    const uint32_t c = __ldg(cp + b);
+    return c >= static_cast<uint32_t>(S - 1) ? S : static_cast<long long>(c) + 1;
+}
+
+// One merge task: head hl of unit u (output row bh = b * H + h), channels
+// [c0, c0 + width) with width a multiple of 8, npieces >= 2 pieces starting at
+// partition c_first.  `sync` is a barrier of the NT threads; it is called the
+// same number of times by all of them.  Shared buffers hold NT entries each.
+template <int NT, typename Sync>
+__device__ __forceinline__ void merge_task(const float *ws_acc, const float2 *ws_ml, void *out,
+                                           int D, int heads_per_cta, long long bh, int c0,
+                                           int width, long long u, int hl, long long c_first,
+                                           int npieces, int tid, float *sm_m, float *sm_l,
+                                           float4 *sm_a, Sync sync) {
+    const int f4 = width / 4;       // float4 per piece row
+    const int nsub = NT / f4;       // pieces in flight
+    const int sub = tid / f4, f = tid - sub * f4;
+    const size_t hgs = static_cast<size_t>(heads_per_cta);
+
+    float M = -INFINITY, L = 0.f;
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (sub < nsub) {
+        for (int j0 = sub; j0 < npieces; j0 += 8 * nsub) {
+            float2 ml[8];
+            float4 v[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int j = j0 + r * nsub;
+                ml[r] = make_float2(-INFINITY, 0.f);
+                v[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (j < npieces) {
+                    const size_t row = static_cast<size_t>(piece_slot(c_first + j, u)) * hgs + hl;
+                    // through L2: the states may come from other CTAs of this grid
+                    ml[r] = __ldcg(ws_ml + row);
+                    v[r] = __ldcg(reinterpret_cast<const float4 *>(ws_acc + row * D + c0 + f * 4));
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) fold(M, L, A, ml[r].x, ml[r].y, v[r]);
+        }
+    }
+    sm_m[tid] = M;
+    sm_l[tid] = L;
+    sm_a[tid] = A;
+    sync();
+    // Level 1: each thread folds one group of eight subs into the group's first
+    // entry; it reads only its own group, so the level needs no barrier inside.
+    const int ngroups = (nsub + 7) / 8;
+    if (tid < ngroups * f4) {
+        const int q = tid / f4, fq = tid - q * f4;
+        const int s_end = min(nsub, q * 8 + 8);
+        const int t0 = q * 8 * f4 + fq;
+        float m2 = sm_m[t0], l2 = sm_l[t0];
+        float4 a2 = sm_a[t0];
+        for (int s2 = q * 8 + 1; s2 < s_end; ++s2) {
+            const int o = s2 * f4 + fq;
+            fold(m2, l2, a2, sm_m[o], sm_l[o], sm_a[o]);
+        }
+        sm_m[t0] = m2;
+        sm_l[t0] = l2;
+        sm_a[t0] = a2;
+    }
+    sync();
+    // Level 2: the group results, then normalise and store f16.
+    if (tid < f4) {
+        float m2 = sm_m[tid], l2 = sm_l[tid];
+        float4 A2 = sm_a[tid];
+        for (int q = 1; q < ngroups; ++q) {
+            const int o = q * 8 * f4 + tid;
+            fold(m2, l2, A2, sm_m[o], sm_l[o], sm_a[o]);
+        }
+        const float inv = 1.f / l2;
+        __half2 lo = __floats2half2_rn(A2.x * inv, A2.y * inv);
+        __half2 hi = __floats2half2_rn(A2.z * inv, A2.w * inv);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t *>(&lo);
+        packed.y = *reinterpret_cast<uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(reinterpret_cast<__half *>(out) + bh * D + c0 + tid * 4) =
+            packed;
+    }
+}
+
+}  // namespace merge
+}  // namespace dattn
