@@ -232,6 +232,14 @@ int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
     const int stage_target = deep ? kStageTargetBytesOnePerSm : kStageTargetBytes;
     int P = std::max(1, std::min(256, stage_target / 2 / row_bytes));
     P = std::max(p.PHI, P / p.PHI * p.PHI);
+    // A batch too small to give every CTA slot two stages takes smaller stages,
+    // for more partitions: such a decode is bound by latency, not by the
+    // per-stage overhead that large stages amortise.
+    {
+        const long long slots = static_cast<long long>(di.sms) * (deep ? 1 : 2);
+        while (P / 2 >= p.PHI && 2 * P > kMinPositions && capacity_pos < slots * 2LL * P)
+            P = std::max(p.PHI, P / 2 / p.PHI * p.PHI);
+    }
     p.P = P;
     const int stage_bytes = 2 * P * row_bytes;
     const int merge_bytes = p.PHI > 1 ? p.HG * p.PHI * (D + 2) * 4 : 0;
