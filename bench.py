@@ -79,7 +79,8 @@ def recorded_traffic(workload: str):
     entry = rec.get(workload)
     if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
         return None
-    return entry.get("dram_bytes_per_call")
+    # a capture of part of a large workload (its first sequences) scales to a full call
+    return entry.get("dram_bytes_per_call") * entry.get("scale", 1)
 
 
 class ClockSampler:
