@@ -56,6 +56,9 @@ SHAPES = [
     (2, 6, 192, 70, [69, 3]),
     (2, 16, 256, 150, [149, 88]),
     (1, 64, 256, 40, [39]),            # two head groups
+    (2, 64, 256, 600, [599, 300]),     # head groups over many full stages (tensor boxes)
+    (2, 80, 256, 301, [300, 41]),      # three groups, the last one smaller (per-position copies)
+    (1, 128, 128, 500, [499]),         # 128 heads at head_dim 128: two groups of 64
     (1, 200, 64, 20, [19]),            # two head groups at head_dim 64
     (3, 1, 8, 1000, [999, 1, 400]),    # one head, many phases
     (5, 2, 128, 1, [0, 0, 7, 0, 0]),   # seq_len 1

@@ -48,7 +48,8 @@ CASES = [
     (2, 32, 128, 1, 300, [299, 150]),
     (3, 40, 128, 7, 30, [209, 13, 100]),
     (2, 4, 48, 64, 3, [191, 70]),
-    (2, 64, 256, 8, 6, [47, 20]),   # two head groups: one copy per position
+    (2, 64, 256, 8, 6, [47, 20]),   # two head groups: tensor boxes inside pages
+    (2, 80, 256, 7, 9, [62, 30]),   # three groups, odd pages: boxes and per-position runs
 ]
 
 
