@@ -268,3 +268,16 @@ def test_workload_outlier_sampled_parity():
         assert_decode_close(out[sl], ref, f"{w.description}, sequence {b}")
     del x
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("partitions", [0, 7])
+@pytest.mark.parametrize("B", [300, 5000])
+def test_large_batches_take_every_prefix_path(B, partitions):
+    # More sequences than threads per CTA: each prologue thread scans several
+    # sequences.  Above 4096 sequences the merge kernel reads the prefix sums
+    # the decode kernel wrote instead of summing current_pos itself.
+    rng = np.random.default_rng(B + partitions)
+    H, D, S = 2, 16, 24
+    cp = rng.integers(0, S + 3, B).tolist()  # some beyond seq_len: nothing masked
+    *_, out, ref = run_case(B, H, D, S, cp, seed=B * 7 + partitions, num_partitions=partitions)
+    assert_decode_close(out, ref, f"B={B} partitions={partitions}")
