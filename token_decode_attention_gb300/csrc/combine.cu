@@ -34,7 +34,13 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kInlinePrefix = 4096;  // batches summed from current_pos in the combine
 
-__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) {
+// INFLIGHT: piece loads each thread issues before folding them.  The host picks
+// the smallest depth that covers a thread's expected pieces in one round; the
+// shallow instances use few registers, so a whole batch's merge CTAs fit the
+// GPU in one wave.
+template <int INFLIGHT>
+__global__ void __launch_bounds__(kThreads, INFLIGHT <= 2 ? 16 : (INFLIGHT <= 4 ? 8 : 1))
+    combine_kernel(const CombineArgs a) {
     __shared__ float sm_m[kThreads], sm_l[kThreads];
     __shared__ float4 sm_a[kThreads];
     __shared__ long long sm_pre[kThreads / 32][2];
@@ -99,7 +105,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineArgs a) 
 
     const int c0 = chunk * a.chunk;
     const int width = min(a.chunk, a.D - c0);  // a multiple of 8
-    merge::merge_task<kThreads>(a.ws_acc, a.ws_ml, a.out, a.D, a.heads_per_cta, bh, c0, width, u,
+    merge::merge_task<kThreads, INFLIGHT>(a.ws_acc, a.ws_ml, a.out, a.D, a.heads_per_cta, bh, c0, width, u,
                                 hl, c_first, npieces, tid, sm_m, sm_l, sm_a,
                                 [] { __syncthreads(); });
 }
@@ -120,7 +126,9 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, a);
+    if (a.inflight <= 2) return cudaLaunchKernelEx(&cfg, combine_kernel<2>, a);
+    if (a.inflight <= 4) return cudaLaunchKernelEx(&cfg, combine_kernel<4>, a);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<8>, a);
 }
 
 }  // namespace dattn

@@ -131,6 +131,7 @@ struct Plan {
     int smem = 0, merge_offset = 0, bar_offset = 0, ctas_per_sm = 0, sms = 0;
     size_t prefix_bytes = 0, acc_bytes = 0, ws_bytes = 0;
     int combine_chunk = 0;  // channels per combine CTA
+    int combine_inflight = 8;  // piece loads per combine thread per round
 };
 
 int next_pow2(int x) {
@@ -278,6 +279,9 @@ int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
         int cw = std::min(256, next_pow2(D));
         while (cw > 8 && pieces * cw / 512.0 > 8.0) cw /= 2;
         p.combine_chunk = cw;
+        // loads in flight per thread: a thread's expected pieces in one round
+        const double per_thread = pieces / (128.0 / (cw / 4));
+        p.combine_inflight = per_thread <= 2.0 ? 2 : (per_thread <= 4.0 ? 4 : 8);
     }
     {
         std::lock_guard<std::mutex> lock(g_plan_mutex);
@@ -357,6 +361,7 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
         c.head_groups = p.NHG;
         c.partitions = p.G;
         c.chunk = p.combine_chunk;
+        c.inflight = p.combine_inflight;
         e = dattn::launch_combine(c, stream);
         if (e != cudaSuccess) return fail_cuda(e, "combine kernel launch");
     }

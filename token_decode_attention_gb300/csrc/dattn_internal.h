@@ -74,7 +74,8 @@ struct CombineArgs {
     int heads_per_cta;
     int head_groups;
     int partitions;
-    int chunk;  // channels per combine CTA (a multiple of 8)
+    int chunk;     // channels per combine CTA (a multiple of 8)
+    int inflight;  // piece loads per thread per round: 2, 4 or 8
 };
 
 // Compile-time shape of one decode-kernel instance.

@@ -1,6 +1,5 @@
 // merge.cuh -- log-sum-exp merge of the pieces of one (sequence, head, chunk
-// of channels), shared by the combine kernel and the decode kernel's fused
-// merge.
+// of channels), the work of one combine CTA.
 //
 // Piece j of a unit left, per head, m_j = max score (log2 units),
 // l_j = sum 2^(s - m_j) and acc_j = sum 2^(s - m_j) V in workspace slot
@@ -8,7 +7,7 @@
 // whole live range is
 //   out = sum_j 2^(m_j - M) acc_j / sum_j 2^(m_j - M) l_j,   M = max_j m_j.
 // NT threads share one task: thread (sub, f) folds pieces sub, sub + nsub, ...
-// of float4 column f online, after issuing the loads of up to eight of them
+// of float4 column f online, after issuing the loads of up to INFLIGHT of them
 // together; the per-thread states are then folded in two levels through shared
 // memory (groups of eight subs, then the group results).
 #pragma once
@@ -59,7 +58,7 @@ __device__ __forceinline__ long long live_len(const uint32_t *cp, long long b, i
 // [c0, c0 + width) with width a multiple of 8, npieces >= 2 pieces starting at
 // partition c_first.  `sync` is a barrier of the NT threads; it is called the
 // same number of times by all of them.  Shared buffers hold NT entries each.
-template <int NT, typename Sync>
+template <int NT, int INFLIGHT, typename Sync>
 __device__ __forceinline__ void merge_task(const float *ws_acc, const float2 *ws_ml, void *out,
                                            int D, int heads_per_cta, long long bh, int c0,
                                            int width, long long u, int hl, long long c_first,
@@ -73,23 +72,23 @@ __device__ __forceinline__ void merge_task(const float *ws_acc, const float2 *ws
     float M = -INFINITY, L = 0.f;
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
     if (sub < nsub) {
-        for (int j0 = sub; j0 < npieces; j0 += 8 * nsub) {
-            float2 ml[8];
-            float4 v[8];
+        for (int j0 = sub; j0 < npieces; j0 += INFLIGHT * nsub) {
+            float2 ml[INFLIGHT];
+            float4 v[INFLIGHT];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
+            for (int r = 0; r < INFLIGHT; ++r) {
                 const int j = j0 + r * nsub;
                 ml[r] = make_float2(-INFINITY, 0.f);
                 v[r] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (j < npieces) {
                     const size_t row = static_cast<size_t>(piece_slot(c_first + j, u)) * hgs + hl;
-                    // through L2: the states may come from other CTAs of this grid
+                    // through L2 (the states were written by the decode kernel's CTAs)
                     ml[r] = __ldcg(ws_ml + row);
                     v[r] = __ldcg(reinterpret_cast<const float4 *>(ws_acc + row * D + c0 + f * 4));
                 }
             }
 #pragma unroll
-            for (int r = 0; r < 8; ++r) fold(M, L, A, ml[r].x, ml[r].y, v[r]);
+            for (int r = 0; r < INFLIGHT; ++r) fold(M, L, A, ml[r].x, ml[r].y, v[r]);
         }
     }
     sm_m[tid] = M;
