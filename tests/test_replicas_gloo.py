@@ -71,3 +71,25 @@ def test_reference_arm_works_on_rank_zero_only():
                        capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_reference_arm_prints_one_contract_line_on_rank_zero():
+    # rank 0 times the oracle on the host cores and prints the JSON line the
+    # driver parses; the small workload keeps the run to a fraction of a second
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "small", "--steps", "2", "--warmup", "3"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    import json
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s"
+    assert line["steps"] == 2 and line["warmup"] == 3 and line["n_gpus"] == 1
+    assert line["higher_is_better"] is True and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    # value = algorithmic bytes of one step / time per step
+    assert line["value"] == pytest.approx(413696 / (line["ms_per_step"] * 1e-3) / 1e9, rel=1e-6)
