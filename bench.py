@@ -306,6 +306,40 @@ class Replica:
         del g
         return ms, clocks
 
+    def step_percentiles(self, samples: int, stream) -> dict:
+        """Latency of one isolated step: one single-step graph per input set
+        (rotating, as in the timed region), each replay bracketed by its own
+        events, so a step neither overlaps its predecessor nor hides its launch;
+        p10 / p50 / p90 in microseconds over `samples` replays.  The headline
+        figure is the back-to-back throughput of the timed region instead."""
+        stream.wait_stream(torch.cuda.current_stream(self.device))
+        graphs = []
+        n = min(self.sets_n, 512)  # 512 of the small workload's sets are 256 MB, 2x L2
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                self.step(i, stream)
+            torch.cuda.synchronize()
+            for i in range(n):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    self.step(i, stream)
+                graphs.append(g)
+            for g in graphs:
+                g.replay()
+            torch.cuda.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(samples)]
+            for k, (a, b) in enumerate(ev):
+                a.record(stream)
+                graphs[k % len(graphs)].replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+        t = np.array([a.elapsed_time(b) * 1e3 for a, b in ev])
+        del graphs
+        return {"p10": float(np.percentile(t, 10)), "p50": float(np.percentile(t, 50)),
+                "p90": float(np.percentile(t, 90)), "samples": samples,
+                "note": "each step its own graph launch (not overlapped with the previous one)"}
+
     def e2e(self, steps: int, warmup: int, stream):
         """Same metric through the public API with host buffers.  Each step copies
         the new token's inputs (q, k, v rows and current_pos, packed in one pinned
@@ -522,11 +556,13 @@ def sweep(device, stream, l2_bytes: int, steps: int, warmup: int, peak: float) -
         try:
             r = Replica(name, device, l2_bytes, page_size=ps)
             ms, _ = r.timed(steps, warmup, stream, 1, soak_s=0.2)
+            pct = r.step_percentiles(max(20, steps), stream)
             t = ms * 1e-3 / steps
             gbs = r.bytes_per_step / t / 1e9
             res[key] = {"us_per_step": t * 1e6, "GB/s": gbs, "frac_of_measured": gbs / peak,
                          "frac_of_nominal_8TBs": gbs / NOMINAL_HBM_GBS,
                          "query_heads_per_s": r.w.batch * r.w.n_heads / t,
+                         "isolated_step_us_p10_p50_p90": [pct["p10"], pct["p50"], pct["p90"]],
                          "partitions": r.plan["partitions"],
                          "algorithmic_bytes": r.bytes_per_step, "l2": r.l2_note}
             del r
@@ -646,6 +682,7 @@ def main():
     t_step = job["t_step"]
     value = job["value_gbs"]
     per_call = rep.bytes_per_step / t_step / 1e9
+    pct = rep.step_percentiles(max(20, args.steps), stream)
     e2e = rep.e2e(args.steps, args.warmup, stream)
     if dattn.dattn_device_error(clear=True) != 0:
         raise RuntimeError("device error word set: a kernel gave up on a pipeline wait")
@@ -679,6 +716,7 @@ def main():
         "submission": "eager Python calls" if args.eager else
                       "one CUDA graph of the K steps, captured before the timed region",
         "eager_ms_per_step": eager_ms / args.steps,
+        "isolated_step_us": pct,
         "gpu_launches": rep.launches_per_step * args.steps,
         "clocks": clocks,
         "plan": rep.plan,
