@@ -455,7 +455,7 @@ def graph_time_us(fn, steps: int, warmup: int, stream, graph: bool = True) -> fl
 
 
 OPS = ["rope_append_7b", "rope_append_ragged", "rope_append_outlier", "softmax_10240x8192",
-       "softmax_65536x1024"]
+       "softmax_65536x1024", "softmax_2048x128256"]
 
 
 def sweep_ops(device, stream, steps: int, warmup: int, peak: float, only: str | None = None,
@@ -498,7 +498,7 @@ def sweep_ops(device, stream, steps: int, warmup: int, peak: float, only: str | 
             import traceback
             traceback.print_exc(file=sys.stderr)
             res[f"rope_append_{name}"] = {"error": f"{type(e).__name__}: {e}"}
-    for rows, cols in ((10240, 8192), (65536, 1024)):
+    for rows, cols in ((10240, 8192), (65536, 1024), (2048, 128256)):
         key = f"softmax_{rows}x{cols}"
         if only is not None and only != key:
             continue

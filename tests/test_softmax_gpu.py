@@ -33,11 +33,15 @@ def check(x: torch.Tensor, out: torch.Tensor):
 
 # widths cover: one warp per row (<= 1024); one CTA per row held in registers
 # (<= 8192) as float4 slots (cols % 4 == 0: 2, 4, 8 per thread) or scalar slots
-# (8, 16, 32 per thread); two passes beyond 8192
+# (8, 16, 32 per thread), and up to 16384 aligned columns with 512 threads;
+# longer aligned rows: persistent CTAs (two per SM up to 65536 columns, one
+# beyond); other long rows: two passes
 @pytest.mark.parametrize("rows,cols", [(1, 1), (7, 5), (64, 32), (33, 1000), (5, 1024),
                                        (9, 1025), (6, 2052), (4, 4096), (2, 6000), (3, 8192),
                                        (5, 3001), (3, 8191), (2, 8193), (2, 8196),
-                                       (2, 131072)])
+                                       (3, 16384), (2, 16388), (3, 24580), (5, 32768),
+                                       (3, 50000), (400, 65536), (3, 65540), (2, 131072),
+                                       (2, 128256), (2, 196612), (2, 200001)])
 def test_softmax_matches_oracle(rows, cols):
     g = torch.Generator(device="cuda").manual_seed(rows * 100003 + cols)
     x = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
@@ -49,7 +53,7 @@ def test_softmax_matches_oracle(rows, cols):
 
 def test_softmax_masked_and_degenerate_rows():
     g = torch.Generator(device="cuda").manual_seed(3)
-    for cols in (300, 5000, 5001, 9000):  # warp per row; CTA per row: float4, scalar, 2 passes
+    for cols in (300, 5000, 5001, 9000, 9001, 60000):  # warp; CTA: float4, scalar; persistent; 2 passes
         x = torch.empty((6, cols), dtype=torch.float32, device="cuda")
         x.normal_(0.0, 3.0, generator=g)
         x[0, ::3] = float("-inf")          # masked entries: weight 0
@@ -76,3 +80,24 @@ def test_softmax_in_place_and_row_sums():
     check(ref, x)
     assert torch.allclose(x.double().sum(dim=1).cpu(), torch.ones(100, dtype=torch.float64),
                           atol=1e-5)
+
+
+def test_softmax_long_rows_with_masked_spans_and_nan():
+    # 60000 columns (the persistent long-row kernel): a span of -infinity gets
+    # weight exactly 0; a NaN inside such a span still turns its row into NaN;
+    # a single live entry takes all the weight.
+    g = torch.Generator(device="cuda").manual_seed(6)
+    x = torch.empty((4, 60000), dtype=torch.float32, device="cuda")
+    x.normal_(0.0, 3.0, generator=g)
+    x[0, 20000:40000] = float("-inf")      # the middle slice masked
+    x[1, 40000:] = float("-inf")           # the last slice masked
+    x[2, 20000:40000] = float("-inf")
+    x[2, 31000] = float("nan")             # ... with a NaN in it
+    x[3, :] = float("-inf")
+    x[3, 59999] = 5.0                      # one live entry in the last slice
+    out = dattn.softmax(x)
+    torch.cuda.synchronize()
+    check(x, out)
+    assert (out[0, 20000:40000] == 0).all() and (out[1, 40000:] == 0).all()
+    assert torch.isnan(out[2]).all()
+    assert abs(float(out[3, 59999]) - 1.0) <= 1e-6 and float(out[3, :59999].abs().max()) == 0.0

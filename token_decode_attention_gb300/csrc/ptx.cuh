@@ -74,6 +74,22 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return true;
 }
 
+// L2 policy for data read again soon: evict last.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 16-byte global load with an L2 cache policy.
+__device__ __forceinline__ float4 ld_f4_hint(const float4 *p, uint64_t policy) {
+    float4 v;
+    asm volatile("ld.global.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
+
 // L2 policy for data read exactly once: evict first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t pol;

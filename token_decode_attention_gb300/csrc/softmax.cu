@@ -8,16 +8,21 @@
 //
 //   short rows (cols <= 1024): one warp per row, the row kept in registers
 //     (32 values per lane), warp-shuffle max and sum: one read, one write;
-//   rows up to 8192: one CTA of 256 threads per row, the row kept in
+//   rows up to 16384: one CTA of 256 or 512 threads per row, the row kept in
 //     registers (up to 32 values per thread), block max and sum through
 //     shared memory: one read, one write;
-//   longer rows: one CTA per row, a pass computing the running (max, sum) per
+//   longer rows (cols % 4 == 0, 16-byte aligned): one or two persistent CTAs
+//     per SM walk the rows; the first pass loads a row with an evict-last L2
+//     policy and computes the running (max, sum) with exp2, the second
+//     re-reads it from L2 and writes the output with streaming stores;
+//   otherwise: one CTA per row, a pass computing the running (max, sum) per
 //     thread merged across the block, then a pass writing the output.
 #include <cuda_runtime.h>
 
 #include <cmath>
 
 #include "dattn_internal.h"
+#include "ptx.cuh"
 
 namespace dattn {
 namespace {
@@ -71,7 +76,7 @@ __global__ void __launch_bounds__(256) softmax_warp_rows(const float *__restrict
 constexpr int kRegRowMax = 32 * kRowThreads;  // columns a CTA holds in registers
 
 // max (IS_MAX) or sum of one value per thread over the CTA; every thread gets it
-template <bool IS_MAX>
+template <bool IS_MAX, int NT = kRowThreads>
 __device__ __forceinline__ float block_all_reduce(float v, float *red) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -82,28 +87,27 @@ __device__ __forceinline__ float block_all_reduce(float v, float *red) {
     __syncthreads();
     v = red[0];
 #pragma unroll
-    for (int w = 1; w < kRowThreads / 32; ++w) v = IS_MAX ? fmaxf(v, red[w]) : v + red[w];
+    for (int w = 1; w < NT / 32; ++w) v = IS_MAX ? fmaxf(v, red[w]) : v + red[w];
     return v;
 }
 
-// One CTA per row, the row in registers: NV slots per thread, a slot being a
-// float4 (VEC, cols % 4 == 0) or a float.  Slot k of thread t covers element
-// (or float4) t + k * kRowThreads, so each load instruction is coalesced.
+// One CTA of NT threads per row, the row in registers: NV slots per thread, a
+// slot being a float4 (VEC, cols % 4 == 0) or a float.  Slot k of thread t
+// covers element (or float4) t + k * NT, so each load instruction is coalesced.
 // Padding is -infinity, which exponentiates to 0.  A NaN anywhere, or a row
 // of -infinity only (max - max = NaN), propagates through the sum to the
 // whole row, as the definition does.
-template <int NV, bool VEC>
-__global__ void __launch_bounds__(kRowThreads) softmax_reg_rows(const float *__restrict__ x,
-                                                                float *__restrict__ out,
-                                                                int cols) {
-    __shared__ float red_m[kRowThreads / 32], red_l[kRowThreads / 32];
+template <int NV, bool VEC, int NT = kRowThreads>
+__global__ void __launch_bounds__(NT) softmax_reg_rows(const float *__restrict__ x,
+                                                       float *__restrict__ out, int cols) {
+    __shared__ float red_m[NT / 32], red_l[NT / 32];
     constexpr int W = VEC ? 4 : 1;
     const long long r = blockIdx.x;
     const int n = VEC ? cols / 4 : cols;
     float v[NV][W];
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-        const int c = threadIdx.x + k * kRowThreads;
+        const int c = threadIdx.x + k * NT;
         if constexpr (VEC) {
             float4 t = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             if (c < n) t = __ldcs(reinterpret_cast<const float4 *>(x + r * cols) + c);
@@ -120,7 +124,7 @@ __global__ void __launch_bounds__(kRowThreads) softmax_reg_rows(const float *__r
     for (int k = 0; k < NV; ++k)
 #pragma unroll
         for (int e = 0; e < W; ++e) m = fmaxf(m, v[k][e]);
-    m = block_all_reduce<true>(m, red_m);
+    m = block_all_reduce<true, NT>(m, red_m);
     float l = 0.f;
 #pragma unroll
     for (int k = 0; k < NV; ++k)
@@ -129,17 +133,132 @@ __global__ void __launch_bounds__(kRowThreads) softmax_reg_rows(const float *__r
             v[k][e] = expf(v[k][e] - m);
             l += v[k][e];
         }
-    l = block_all_reduce<false>(l, red_l);
+    l = block_all_reduce<false, NT>(l, red_l);
     const float inv = 1.f / l;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-        const int c = threadIdx.x + k * kRowThreads;
+        const int c = threadIdx.x + k * NT;
         if (c < n) {
             if constexpr (VEC)
                 __stcs(reinterpret_cast<float4 *>(out + r * cols) + c,
                        make_float4(v[k][0] * inv, v[k][1] * inv, v[k][2] * inv, v[k][3] * inv));
             else
                 __stcs(out + r * cols + c, v[k][0] * inv);
+        }
+    }
+}
+
+// ---- long rows, persistent: one CTA per SM walks the rows, and the second
+// pass finds the row in L2 ----
+constexpr int kL2Threads = 1024;
+constexpr int kL2Unroll = 4;  // float4 loads in flight per thread
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// merge() for states whose sums are 2^(x log2(e) - S(m)), S(m) = m log2(e)
+__device__ __forceinline__ void merge2(float &m, float &l, float m2, float l2) {
+    const float M = fmaxf(m, m2);
+    if (M == -INFINITY) return;
+    const float sM = __fmul_rn(M, kLog2e);
+    l = l * ex2(__fmul_rn(m, kLog2e) - sM) + l2 * ex2(__fmul_rn(m2, kLog2e) - sM);
+    m = M;
+}
+
+// A row is read twice, but by at most one CTA per SM at a time, so the rows in
+// flight (SMs x row bytes) stay within L2: the first pass loads with an
+// evict-last policy and computes the running (max, sum of exp); the second
+// pass re-reads the row (evict-first), normalises and writes with streaming
+// stores.  One HBM read and one write per element when the rows in flight fit
+// L2.
+template <int NT>
+__global__ void __launch_bounds__(NT, kL2Threads / NT) softmax_l2_rows(const float *__restrict__ x,
+                                                                        float *__restrict__ out,
+                                                                        long long rows, int cols) {
+    __shared__ float sm_m[NT / 32], sm_l[NT / 32];
+    __shared__ int sm_nan[NT / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n4 = cols / 4;
+    const uint64_t keep = l2_evict_last_policy();
+    const uint64_t drop = l2_evict_first_policy();
+    for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(x + r * cols);
+        float m = -INFINITY, l = 0.f;
+        bool nan = false;
+        for (int c = tid; c < n4; c += NT * kL2Unroll) {
+            float4 t[kL2Unroll];
+#pragma unroll
+            for (int k = 0; k < kL2Unroll; ++k) {
+                const int ck = c + k * NT;
+                t[k] = ck < n4 ? ld_f4_hint(x4 + ck, keep)
+                               : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+#pragma unroll
+            for (int k = 0; k < kL2Unroll; ++k) {
+                // m is kept in x units and S(m) = m log2(e) rounded once; a term is
+                // 2^(x log2(e) - S(m)) with the difference formed by one fused
+                // multiply-add, so S(m)'s rounding is common to every term and
+                // cancels in the normalisation.  Rescale only when m rises.
+                nan |= isnan(t[k].x) || isnan(t[k].y) || isnan(t[k].z) || isnan(t[k].w);
+                const float M = fmaxf(m, fmaxf(fmaxf(t[k].x, t[k].y), fmaxf(t[k].z, t[k].w)));
+                if (M != -INFINITY) {
+                    const float sM = __fmul_rn(M, kLog2e);
+                    if (M > m) {
+                        l *= ex2(__fmul_rn(m, kLog2e) - sM);  // 0 while m is -inf
+                        m = M;
+                    }
+                    l += ex2(fmaf(t[k].x, kLog2e, -sM)) + ex2(fmaf(t[k].y, kLog2e, -sM)) +
+                         ex2(fmaf(t[k].z, kLog2e, -sM)) + ex2(fmaf(t[k].w, kLog2e, -sM));
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+            const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+            merge2(m, l, m2, l2);
+        }
+        const bool warp_nan = __any_sync(0xffffffffu, nan);
+        if (lane == 0) {
+            sm_m[warp] = m;
+            sm_l[warp] = l;
+            sm_nan[warp] = warp_nan;
+        }
+        __syncthreads();
+        m = sm_m[0];
+        l = sm_l[0];
+        bool row_nan = sm_nan[0];
+#pragma unroll
+        for (int w = 1; w < NT / 32; ++w) {
+            merge2(m, l, sm_m[w], sm_l[w]);
+            row_nan |= sm_nan[w] != 0;
+        }
+        __syncthreads();  // the shared states are read before the next row writes them
+        // a NaN anywhere, or a row of -infinity only, gives a NaN row
+        if (row_nan) l = NAN;
+        const float inv = 1.f / l;
+        const float sm = __fmul_rn(m, kLog2e);
+        float4 *o4 = reinterpret_cast<float4 *>(out + r * cols);
+        for (int c = tid; c < n4; c += NT * kL2Unroll) {
+            float4 t[kL2Unroll];
+#pragma unroll
+            for (int k = 0; k < kL2Unroll; ++k) {
+                const int ck = c + k * NT;
+                if (ck < n4) t[k] = ld_f4_hint(x4 + ck, drop);
+            }
+#pragma unroll
+            for (int k = 0; k < kL2Unroll; ++k) {
+                const int ck = c + k * NT;
+                if (ck < n4)
+                    __stcs(o4 + ck, make_float4(ex2(fmaf(t[k].x, kLog2e, -sm)) * inv,
+                                                ex2(fmaf(t[k].y, kLog2e, -sm)) * inv,
+                                                ex2(fmaf(t[k].z, kLog2e, -sm)) * inv,
+                                                ex2(fmaf(t[k].w, kLog2e, -sm)) * inv));
+            }
         }
     }
 }
@@ -232,6 +351,18 @@ cudaError_t launch_softmax(const float *x, float *out, long long rows, int cols,
     if (rows > 0x7fffffffLL) return cudaErrorInvalidValue;
     bool vec4 = (cols % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) &&
                 ((reinterpret_cast<uintptr_t>(out) & 15u) == 0);
+#ifndef DATTN_SOFTMAX_REG_MAX
+#define DATTN_SOFTMAX_REG_MAX (2 * kRegRowMax)  // widest row held in registers (<= 32768)
+#endif
+    if (vec4 && cols > kRegRowMax && cols <= DATTN_SOFTMAX_REG_MAX) {
+        // 512 or 1024 threads of 8 float4 each: the row still in registers
+        void *args[] = {&x, &out, &cols};
+        const void *fn = cols <= 2 * kRegRowMax
+                             ? reinterpret_cast<const void *>(softmax_reg_rows<8, true, 512>)
+                             : reinterpret_cast<const void *>(softmax_reg_rows<8, true, 1024>);
+        return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(rows)),
+                                dim3(cols <= 2 * kRegRowMax ? 512 : 1024), args, 0, stream);
+    }
     if (cols <= kRegRowMax) {
         // smallest register footprint that holds the row
         const int per_thread = (cols + kRowThreads - 1) / kRowThreads;  // 5 .. 32 floats
@@ -248,6 +379,23 @@ cudaError_t launch_softmax(const float *x, float *out, long long rows, int cols,
         void *args[] = {&x, &out, &cols};
         return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(rows)), dim3(kRowThreads), args, 0,
                                 stream);
+    }
+    if (vec4) {
+        // long aligned rows: one or two persistent CTAs per SM walk the rows
+        int sms = 0, dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        // two CTAs of 512 threads per SM while two rows per SM still fit L2,
+        // else one of 1024
+        const bool two = static_cast<long long>(cols) * 4 <= 256 * 1024;
+        const long long slots = static_cast<long long>(sms) * (two ? 2 : 1);
+        const long long grid = rows < slots ? rows : slots;
+        void *args[] = {&x, &out, &rows, &cols};
+        return cudaLaunchKernel(two ? reinterpret_cast<const void *>(softmax_l2_rows<512>)
+                                    : reinterpret_cast<const void *>(softmax_l2_rows<1024>),
+                                dim3(static_cast<unsigned>(grid)), dim3(two ? 512 : 1024), args,
+                                0, stream);
     }
     void *args[] = {&x, &out, &cols, &vec4};
     return cudaLaunchKernel(reinterpret_cast<const void *>(softmax_block_rows),
