@@ -58,10 +58,15 @@ def hbm_peak() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# the sources of the decode call whose DRAM traffic profiles/ncu_traffic.json records
+DECODE_SOURCES = ("decode_streamk.cu", "combine.cu", "merge.cuh", "streamk.h", "ptx.cuh",
+                  "dattn_internal.h", "dattn_api.cpp")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "token_decode_attention_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in DECODE_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
