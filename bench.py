@@ -529,11 +529,15 @@ def sweep_ops(device, stream, steps: int, warmup: int, peak: float, only: str | 
     return res
 
 
-def cpu_baseline(name: str, budget_s: float, max_reps: int = 1000) -> dict:
-    """The CPU oracle, as it stands, on a bounded sample of the workload."""
+def cpu_baseline(name: str, budget_s: float, max_reps: int = 1000, batch: int = 0) -> dict:
+    """The CPU oracle, as it stands, on a bounded sample of the workload
+    (`batch` > 0: that many sequences of the same recipe)."""
     import oracle
     w = WORKLOADS[name]
-    x = make_inputs(w, "cuda")
+    if batch:
+        import dataclasses
+        w = dataclasses.replace(w, batch=batch)
+    x = make_inputs(WORKLOADS[name], "cuda", batch=w.batch)
     q, k, v = (x[n].cpu().numpy() for n in ("q", "k", "v"))
     cp = x["cur_pos_host"]
     del x
@@ -548,8 +552,24 @@ def cpu_baseline(name: str, budget_s: float, max_reps: int = 1000) -> dict:
     return {"value": nbytes * reps / el / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
             "kind": "oracle", "seconds": el,
             "query_heads_per_s": w.batch * w.n_heads * reps / el,
-            "sample": f"{reps} full passes of the {name} workload ({w.description}), "
-                      f"fp64 C oracle with OpenMP"}
+            "sample": f"{reps} full passes of the {name} workload ({w.description})"
+                      + (f", {w.batch} of its sequences" if batch else "")
+                      + ", fp64 C oracle with OpenMP"}
+
+
+def cpu_sweep(budget_s: float) -> dict:
+    """The oracle on every workload: small to long whole, outlier on 16 of its
+    256 sequences (40 GiB of K/V would not fit a bounded run)."""
+    res = {}
+    for name in ("small", "7b", "ragged", "long", "outlier"):
+        try:
+            r = cpu_baseline(name, budget_s, batch=16 if name == "outlier" else 0)
+            res[name] = {k: r[k] for k in ("value", "unit", "query_heads_per_s", "seconds",
+                                           "cores", "sample")}
+        except Exception as e:
+            res[name] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.empty_cache()
+    return res
 
 
 def sweep(device, stream, l2_bytes: int, steps: int, warmup: int, peak: float) -> dict:
@@ -733,6 +753,7 @@ def main():
         if not args.no_sweep:
             line["sweep"] = sweep(device, stream, l2, 20, 3, peak)
             line["sweep_ops"] = sweep_ops(device, stream, 20, 3, peak)
+            line["cpu_sweep"] = cpu_sweep(min(3.0, args.cpu_seconds))
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
