@@ -65,6 +65,7 @@ int main() {
             // walk the pieces partition by partition, as the kernels do
             std::set<long long> slots;
             std::vector<long long> first(U, -1), last(U, -1);
+            std::vector<std::set<long long>> holders(U);
             for (long long c = 0; c < G; ++c) {
                 long long x = range_begin(c, W, G);
                 const long long x1 = range_begin(c + 1, W, G);
@@ -84,6 +85,7 @@ int main() {
                     if (!slots.insert(s).second) return fail("slot unique", c, u);
                     if (first[u] < 0) first[u] = c;
                     last[u] = c;
+                    holders[u].insert(c);
                     x += len;
                 }
             }
@@ -93,6 +95,14 @@ int main() {
                     const long long Pu = NHG * Pb[b] + g * L[b];
                     if (range_owner(Pu, W, G) != first[u]) return fail("first owner", u, G);
                     if (range_owner(Pu + L[b] - 1, W, G) != last[u]) return fail("last owner", u, G);
+                    // between its first and last partition, a unit's pieces are held
+                    // exactly by the partitions whose range is not empty (the merge
+                    // skips the empty ones, which exist only when W < G)
+                    for (long long c = first[u]; c <= last[u]; ++c) {
+                        const bool empty = range_begin(c + 1, W, G) == range_begin(c, W, G);
+                        if (empty == (holders[u].count(c) != 0)) return fail("holders", u, c);
+                        if (empty && W >= G) return fail("empty range with W >= G", c, W);
+                    }
                 }
             }
         }

@@ -281,3 +281,25 @@ def test_large_batches_take_every_prefix_path(B, partitions):
     cp = rng.integers(0, S + 3, B).tolist()  # some beyond seq_len: nothing masked
     *_, out, ref = run_case(B, H, D, S, cp, seed=B * 7 + partitions, num_partitions=partitions)
     assert_decode_close(out, ref, f"B={B} partitions={partitions}")
+
+
+@pytest.mark.parametrize("B,H,D,S,cp,partitions", [
+    (2, 1, 112, 478, [89, 178], 288),     # W = 269 live positions < 288 partitions
+    (4, 8, 64, 64, [0, 3, 1, 10], 40),    # W = 19 < 40
+    (6, 4, 128, 512, [0, 0, 2, 0, 7, 1], 0),  # W = 16: fewer live positions than the plan's CTAs
+    (2, 1, 112, 478, [89, 178], 100),     # W > G: every range holds positions
+])
+def test_empty_partitions_are_skipped_whatever_the_workspace_holds(B, H, D, S, cp, partitions):
+    # With fewer live positions than partitions some ranges are empty, and an
+    # empty one can lie between a sequence's first and last partition.  Its
+    # workspace slot is not written by this call, so the merge must skip it:
+    # the workspace is poisoned with NaN bytes first, and the result must still
+    # match the oracle.
+    g = torch.Generator(device="cuda").manual_seed(B * 31 + partitions)
+    q, k, v = rand_f16(g, (B, H, D)), rand_f16(g, (B, S, H, D)), rand_f16(g, (B, S, H, D))
+    n = max(16, dattn.dattn_decode_workspace_bytes(B, H, D, S, partitions))
+    ws = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")  # every float NaN
+    out = dattn.decode(q, k, v, cur_pos_tensor(cp), num_partitions=partitions, workspace=ws)
+    torch.cuda.synchronize()
+    ref = oracle.decode_f64(to_np(q), to_np(k), to_np(v), np.asarray(cp, np.uint32))
+    assert_decode_close(out, ref, f"W={sum(min(c, S - 1) + 1 for c in cp)} G={partitions}")

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, INFLIGHT <= 2 ? 16 : (INFLIGHT <= 4 
     const int c0 = chunk * a.chunk;
     const int width = min(a.chunk, a.D - c0);  // a multiple of 8
     merge::merge_task<kThreads, INFLIGHT>(a.ws_acc, a.ws_ml, a.out, a.D, a.heads_per_cta, bh, c0, width, u,
-                                hl, c_first, npieces, tid, sm_m, sm_l, sm_a,
+                                hl, c_first, npieces, W, a.partitions, tid, sm_m, sm_l, sm_a,
                                 [] { __syncthreads(); });
 }
 

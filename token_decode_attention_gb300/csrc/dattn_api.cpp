@@ -236,7 +236,10 @@ int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
     // A batch too small to give every CTA slot two stages takes smaller stages,
     // for more partitions: such a decode is bound by latency, not by the
     // per-stage overhead that large stages amortise.
-    {
+#ifndef DATTN_SMALL_BATCH_STAGES
+#define DATTN_SMALL_BATCH_STAGES 1
+#endif
+    if (DATTN_SMALL_BATCH_STAGES) {
         const long long slots = static_cast<long long>(di.sms) * (deep ? 1 : 2);
         while (P / 2 >= p.PHI && 2 * P > kMinPositions && capacity_pos < slots * 2LL * P)
             P = std::max(p.PHI, P / 2 / p.PHI * p.PHI);

@@ -55,15 +55,19 @@ __device__ __forceinline__ long long live_len(const uint32_t *cp, long long b, i
 }
 
 // One merge task: head hl of unit u (output row bh = b * H + h), channels
-// [c0, c0 + width) with width a multiple of 8, npieces >= 2 pieces starting at
-// partition c_first.  `sync` is a barrier of the NT threads; it is called the
-// same number of times by all of them.  Shared buffers hold NT entries each.
+// [c0, c0 + width) with width a multiple of 8, over partitions c_first ..
+// c_first + npieces - 1 (npieces >= 2) of the W flattened positions cut into G
+// ranges.  When W < G some ranges are empty and may lie between the unit's
+// first and last partition: those partitions hold no piece (their slots were
+// not written by this launch) and are skipped.  `sync` is a barrier of the NT
+// threads; it is called the same number of times by all of them.  Shared
+// buffers hold NT entries each.
 template <int NT, int INFLIGHT, typename Sync>
 __device__ __forceinline__ void merge_task(const float *ws_acc, const float2 *ws_ml, void *out,
                                            int D, int heads_per_cta, long long bh, int c0,
                                            int width, long long u, int hl, long long c_first,
-                                           int npieces, int tid, float *sm_m, float *sm_l,
-                                           float4 *sm_a, Sync sync) {
+                                           int npieces, long long W, long long G, int tid,
+                                           float *sm_m, float *sm_l, float4 *sm_a, Sync sync) {
     const int f4 = width / 4;       // float4 per piece row
     const int nsub = NT / f4;       // pieces in flight
     const int sub = tid / f4, f = tid - sub * f4;
@@ -80,8 +84,10 @@ __device__ __forceinline__ void merge_task(const float *ws_acc, const float2 *ws
                 const int j = j0 + r * nsub;
                 ml[r] = make_float2(-INFINITY, 0.f);
                 v[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (j < npieces) {
-                    const size_t row = static_cast<size_t>(piece_slot(c_first + j, u)) * hgs + hl;
+                const long long c = c_first + j;
+                // every range holds at least one position when W >= G
+                if (j < npieces && (W >= G || range_begin(c + 1, W, G) > range_begin(c, W, G))) {
+                    const size_t row = static_cast<size_t>(piece_slot(c, u)) * hgs + hl;
                     // through L2 (the states were written by the decode kernel's CTAs)
                     ml[r] = __ldcg(ws_ml + row);
                     v[r] = __ldcg(reinterpret_cast<const float4 *>(ws_acc + row * D + c0 + f * 4));
