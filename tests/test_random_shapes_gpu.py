@@ -1,10 +1,11 @@
 """Seeded random shapes, dense and paged, against the fp64 oracle.
 
-Forty cases drawn from one seed: every head_dim class (multiples of 8 up to
-256), head counts up to 80 (head groups included), ragged current_pos (some
-beyond seq_len), the library's partition count or a forced one, and half of
-them through a paged cache with a shuffled block table.  Sizes stay small
-enough for the oracle (B*S*H*D <= 2e7).
+A hundred cases drawn from one seed: every head_dim class (multiples of 8 up
+to 256), head counts up to 80 (head groups included), ragged current_pos (some
+beyond seq_len), the library's partition count or a forced one (often more
+partitions than live positions, so some ranges are empty), and half of them
+through a paged cache with a shuffled block table.  Sizes stay small enough for
+the oracle (B*S*H*D <= 1.2e7).
 """
 from __future__ import annotations
 
@@ -21,7 +22,7 @@ from ._util import assert_decode_close, cur_pos_tensor, rand_f16, to_np
 pytestmark = pytest.mark.gpu
 
 
-def draw_cases(n=40, seed=20260101):
+def draw_cases(n=100, seed=20260101):
     rng = np.random.default_rng(seed)
     cases = []
     while len(cases) < n:
@@ -29,10 +30,17 @@ def draw_cases(n=40, seed=20260101):
         H = int(rng.choice([1, 2, 3, 5, 8, 12, 32, 40, 64, 80]))
         B = int(rng.integers(1, 7))
         S = int(rng.integers(1, 1500))
-        if B * S * H * D > 2e7:
+        if B * S * H * D > 1.2e7:
             continue
         cp = rng.integers(0, S + 3, B).tolist()
-        partitions = 0 if rng.random() < 0.5 else int(rng.integers(1, 301))
+        live = sum(min(c, S - 1) + 1 for c in cp)
+        r = rng.random()
+        if r < 0.4:
+            partitions = 0
+        elif r < 0.7:  # more partitions than live positions: empty ranges
+            partitions = int(rng.integers(live + 1, live + 300))
+        else:
+            partitions = int(rng.integers(1, 301))
         ps = int(rng.choice([1, 3, 8, 16, 64])) if rng.random() < 0.5 else 0
         cases.append((B, H, D, S, cp, partitions, ps, len(cases)))
     return cases
