@@ -101,3 +101,32 @@ def test_softmax_long_rows_with_masked_spans_and_nan():
     assert (out[0, 20000:40000] == 0).all() and (out[1, 40000:] == 0).all()
     assert torch.isnan(out[2]).all()
     assert abs(float(out[3, 59999]) - 1.0) <= 1e-6 and float(out[3, :59999].abs().max()) == 0.0
+
+
+def _random_softmax_cases(n=40, seed=20260202):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        cols = int(rng.choice([int(rng.integers(1, 1100)), int(rng.integers(1000, 20000)),
+                               int(rng.integers(16000, 70000))]))
+        rows = int(max(1, min(int(rng.integers(1, 300)), 4e6 // cols)))
+        cases.append((rows, cols, bool(rng.random() < 0.3), i))  # 30 %: not 16-byte aligned
+    return cases
+
+
+@pytest.mark.parametrize("rows,cols,shifted,i", _random_softmax_cases(),
+                         ids=[f"{c[3]}-{c[0]}x{c[1]}{'-shift' if c[2] else ''}"
+                              for c in _random_softmax_cases()])
+def test_softmax_random_shapes(rows, cols, shifted, i):
+    # seeded widths across every path; "shifted" matrices start one float past a
+    # 16-byte boundary, which takes the scalar forms
+    g = torch.Generator(device="cuda").manual_seed(4000 + i)
+    n = rows * cols
+    buf = torch.empty((n + 1,), dtype=torch.float32, device="cuda")
+    buf.normal_(0.0, 5.0, generator=g)
+    x = buf[1:].view(rows, cols) if shifted else buf[:n].view(rows, cols)
+    obuf = torch.empty_like(buf)
+    out = obuf[1:].view(rows, cols) if shifted else obuf[:n].view(rows, cols)
+    dattn.dattn_softmax_f32(x, out)
+    torch.cuda.synchronize()
+    check(x, out)
