@@ -147,8 +147,10 @@ int dattn_decode_f16_ex(const void *Q, const void *K_cache, const void *V_cache,
  * by the library, one per (device, stream), grown on demand with cudaMalloc
  * (serialised by a mutex) and kept until process exit; a call that has to grow
  * it synchronises the device first.  Make the first call for the largest shape
- * outside any CUDA graph capture.
- * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, CUDA.
+ * outside any CUDA graph capture: a call that would have to grow the workspace
+ * while its stream is being captured returns DATTN_ERR_WORKSPACE and leaves the
+ * capture intact.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA.
  */
 int dattn_decode_f16(const void *Q, const void *K_cache, const void *V_cache, void *out,
                      int batch, int n_heads, int head_dim, int seq_len,
