@@ -279,8 +279,11 @@ int dattn_rope_append_paged_f16(const void *q_new, const void *k_new, const void
  * max-subtracted softmax of the decode path's reduction on its own:
  *   out[r, c] = exp(x[r, c] - max_c x[r, c]) / sum_c exp(x[r, c] - max_c x[r, c])
  *   x, out  [rows, cols] f32, device, row-major, 4-byte aligned (out may equal x)
- * computed in fp32 (expf).  -infinity entries get weight 0; a row with a NaN,
- * or with every entry -infinity, comes out NaN, as the definition gives.
+ * computed in fp32: expf for rows up to 16384 columns; longer rows whose width
+ * is a multiple of 4 and whose pointers are 16-byte aligned use exp2 of the
+ * log2(e)-scaled difference formed by one fused multiply-add (relative error
+ * about 1e-6).  -infinity entries get weight 0; a row with a NaN, or with every
+ * entry -infinity, comes out NaN, as the definition gives.
  * Errors: INVALID_ARG, MISALIGNED, UNSUPPORTED, CUDA.
  */
 int dattn_softmax_f32(const float *x, float *out, long long rows, int cols,
