@@ -48,6 +48,9 @@ constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
 #ifndef DATTN_DEEP_RING_POSITIONS
 #define DATTN_DEEP_RING_POSITIONS (1LL << 40)
 #endif
+#ifndef DATTN_PREFETCH_STAGES
+#define DATTN_PREFETCH_STAGES 3  // stages each CTA prefetches into L2 before its wait (0: none)
+#endif
 #ifndef DATTN_MIN_HEAD_GROUPS
 #define DATTN_MIN_HEAD_GROUPS 1  // split the heads into at least this many groups
 #endif
@@ -347,6 +350,11 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
     a.merge_offset = p.merge_offset;
     a.bar_offset = p.bar_offset;
     a.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    // dense caches with one head group: prefetch the first stages into L2 before
+    // the wait on the previous kernel
+    a.prefetch_positions = (DATTN_PREFETCH_STAGES > 0 && pg.table == nullptr && p.NHG == 1)
+                               ? DATTN_PREFETCH_STAGES * p.P
+                               : 0;
     cudaError_t e = dattn::launch_decode(a, p.v, p.smem, stream);
     if (e != cudaSuccess) return fail_cuda(e, "decode kernel launch");
     if (p.G > 1) {

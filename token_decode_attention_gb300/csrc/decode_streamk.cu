@@ -179,6 +179,32 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     // is touched, so this CTA may already be resident while the kernel before it
     // on the stream finishes.  Everything after the wait sees that kernel's writes
     // (current_pos, Q, the cache).
+    //
+    // Before waiting, thread 0 prefetches into L2 the first positions of the
+    // range this CTA would own if every sequence were full (the range depends on
+    // current_pos, which may not be final yet).  Kernel parameters alone give
+    // that range, so nothing the previous kernel writes is read; a prefetch only
+    // warms L2, the point of coherence, so the reads after the wait still see
+    // the final data.  Exact when the caches are full; elsewhere some of it is
+    // read by other CTAs, the rest is wasted bandwidth.
+    if (threadIdx.x == 0 && a.prefetch_positions > 0) {
+        const long long S = a.S;
+        const long long Wc = static_cast<long long>(a.B) * S;  // capacity: the host keeps c * Wc in 64 bits
+        long long x = static_cast<long long>(blockIdx.x) * Wc / a.partitions;
+        const long long x_end =
+            min(x + a.prefetch_positions, static_cast<long long>(blockIdx.x + 1) * Wc / a.partitions);
+        const size_t row = static_cast<size_t>(a.H) * a.D;  // halves per position
+        while (x < x_end) {
+            const long long b = x / S;
+            const long long off = x - b * S;
+            const long long n = min(S - off, x_end - x);
+            const size_t first = static_cast<size_t>(b * S + off) * row;
+            const uint32_t bytes = static_cast<uint32_t>(n * row * 2);
+            bulk_prefetch_l2(reinterpret_cast<const __half *>(a.K) + first, bytes);
+            bulk_prefetch_l2(reinterpret_cast<const __half *>(a.V) + first, bytes);
+            x += n;
+        }
+    }
     pdl_wait_primary();
 
     // ---- the CTA's range: block scan of the live lengths over the batch ----

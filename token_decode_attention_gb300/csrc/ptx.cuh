@@ -109,6 +109,13 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16) of global memory into L2.  A hint:
+// it moves no data into the CTA and cannot make a later read see stale values
+// (L2 is the point of coherence).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch: let the next kernel on the stream start
 // launching, and (in that kernel) wait until the previous grid has completed
 // and its memory is visible.
