@@ -48,6 +48,9 @@ constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
 #ifndef DATTN_DEEP_RING_POSITIONS
 #define DATTN_DEEP_RING_POSITIONS (1LL << 40)
 #endif
+#ifndef DATTN_MIN_CONSUMER_WARPS
+#define DATTN_MIN_CONSUMER_WARPS 8  // 16: always sixteen consumer warps per CTA
+#endif
 #ifndef DATTN_PREFETCH_STAGES
 #define DATTN_PREFETCH_STAGES 3  // stages each CTA prefetches into L2 before its wait (0: none)
 #endif
@@ -213,7 +216,7 @@ int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
     // slots; otherwise sixteen (one CTA per SM, same warps per SM); beyond that
     // the heads are split into groups handled by different CTAs.
     const int kcap = ch == 2 ? 1 : 2;  // register slots per lane group
-    int nwc = 8;
+    int nwc = DATTN_MIN_CONSUMER_WARPS > 8 ? 16 : 8;
     if (H > nwc * (32 / bdx) * kcap) nwc = 16;
     const int nlg = nwc * (32 / bdx);  // lane groups per CTA
     const int hg_max = std::min(nlg * kcap, std::max(1, kMaxRowBytesKV / (D * 4)));

@@ -37,6 +37,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <type_traits>
 
 #include "dattn_internal.h"
 #include "ptx.cuh"
@@ -150,6 +151,7 @@ __device__ __forceinline__ bool next_piece(Walker &w, const DecodeArgs &a) {
 template <int BDX, int CH, int KMAX, int NWC>
 __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     decode_streamk_kernel(const DecodeArgs a) {
+    constexpr int NPOS = 2;              // positions per (head, phase) slot in a consumer group
     constexpr int BDY = 32 / BDX;        // lane groups per warp
     constexpr int NLG = NWC * BDY;       // lane groups per CTA
     constexpr int kThreads = decode_threads(NWC);
@@ -389,6 +391,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     bool con[CH];
 #pragma unroll
     for (int i = 0; i < CH; ++i) con[i] = lig + BDX * i < nchunk;
+    const bool all_con = BDX * CH == nchunk;  // every lane owns all its chunks
 
     int hl[KMAX], ph[KMAX];
 #pragma unroll
@@ -412,16 +415,19 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         const int h0 = walk.g * a.heads_per_cta;
         const int hg = min(a.heads_per_cta, a.H - h0);
         const bool final_piece = (walk.off == 0 && walk.len == walk.Lb);
+        const int pstride = a.phases * hg * D;  // halves between a slot's consecutive positions
         const long long slot_id = piece_slot(blockIdx.x, walk.u);
         const __half *Qb =
             reinterpret_cast<const __half *>(a.Q) + (static_cast<size_t>(walk.b) * a.H + h0) * D;
 
         bool sv[KMAX];
+        int kofs[KMAX];  // halves from a stage's first row to the slot's first row
         uint4 q[KMAX][CH];
         float acc[KMAX][CH * 8], m[KMAX], l[KMAX];
 #pragma unroll
         for (int k = 0; k < KMAX; ++k) {
             sv[k] = ph[k] < a.phases && hl[k] < hg;
+            kofs[k] = sv[k] ? (ph[k] * hg + hl[k]) * D : 0;
             m[k] = -INFINITY;
             l[k] = 0.f;
 #pragma unroll
@@ -448,44 +454,58 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
             const int np = min(a.stage_pos, walk.len - p);
             const __half *sK = ring + static_cast<size_t>(slot) * 2 * buf_elems;
             const __half *sV = sK + buf_elems;
-            for (int t = 0; t < iters; t += 2) {
-                float s0[KMAX], s1[KMAX];
-                bool v0[KMAX], v1[KMAX];
-                int r0[KMAX], r1[KMAX];
+            // One group: NPOS positions of each (head, phase) slot, whose dot
+            // products, shuffles and exponentials are independent, so their
+            // latencies overlap.  CHK = false is the path of a full group (every
+            // position of it inside the stage, every chunk of the row owned):
+            // no per-position tests.  A lane group without a slot still runs it,
+            // on rows of the stage (kofs = 0), and its state is never written.
+            auto group = [&](const int t, auto checked) {
+                constexpr bool CHK = decltype(checked)::value;
+                float s[KMAX][NPOS];
+                bool vv[KMAX][NPOS];
+                int rr[KMAX][NPOS];
 #pragma unroll
                 for (int k = 0; k < KMAX; ++k) {
-                    const int j0 = ph[k] + t * a.phases;
-                    const int j1 = j0 + a.phases;
-                    v0[k] = sv[k] && j0 < np;
-                    v1[k] = sv[k] && (t + 1 < iters) && j1 < np;
-                    r0[k] = (j0 * hg + hl[k]) * D;
-                    r1[k] = (j1 * hg + hl[k]) * D;
-                    float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
+                    float a_[NPOS], b_[NPOS];
+#pragma unroll
+                    for (int n = 0; n < NPOS; ++n) {
+                        vv[k][n] = !CHK || (sv[k] && (t + n < iters) && ph[k] + (t + n) * a.phases < np);
+                        rr[k][n] = kofs[k] + (t + n) * pstride;
+                        a_[n] = 0.f;
+                        b_[n] = 0.f;
+                    }
 #pragma unroll
                     for (int i = 0; i < CH; ++i) {
-                        if (con[i]) {
+                        if (!CHK || con[i]) {
                             const int c8 = (lig + BDX * i) * 8;
-                            if (v0[k]) dot8(q[k][i], *reinterpret_cast<const uint4 *>(sK + r0[k] + c8), a0, b0);
-                            if (v1[k]) dot8(q[k][i], *reinterpret_cast<const uint4 *>(sK + r1[k] + c8), a1, b1);
+#pragma unroll
+                            for (int n = 0; n < NPOS; ++n)
+                                if (vv[k][n])
+                                    dot8(q[k][i], *reinterpret_cast<const uint4 *>(sK + rr[k][n] + c8),
+                                         a_[n], b_[n]);
                         }
                     }
-                    s0[k] = a0 + b0;
-                    s1[k] = a1 + b1;
+#pragma unroll
+                    for (int n = 0; n < NPOS; ++n) s[k][n] = a_[n] + b_[n];
                 }
 #pragma unroll
                 for (int o = BDX / 2; o > 0; o >>= 1) {
 #pragma unroll
-                    for (int k = 0; k < KMAX; ++k) {
-                        s0[k] += __shfl_xor_sync(kFull, s0[k], o);
-                        s1[k] += __shfl_xor_sync(kFull, s1[k], o);
-                    }
+                    for (int k = 0; k < KMAX; ++k)
+#pragma unroll
+                        for (int n = 0; n < NPOS; ++n) s[k][n] += __shfl_xor_sync(kFull, s[k][n], o);
                 }
 #pragma unroll
                 for (int k = 0; k < KMAX; ++k) {
-                    if (!v0[k]) continue;  // v1 implies v0
-                    const float sc0 = s0[k] * a.qscale;
-                    const float sc1 = v1[k] ? s1[k] * a.qscale : -INFINITY;
-                    const float mx = fmaxf(sc0, sc1);
+                    if (CHK && !vv[k][0]) continue;  // a later position valid implies the first
+                    float sc[NPOS];
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int n = 0; n < NPOS; ++n) {
+                        sc[n] = vv[k][n] ? s[k][n] * a.qscale : -INFINITY;
+                        mx = fmaxf(mx, sc[n]);
+                    }
                     if (mx > m[k]) {  // new running max: rescale the state
                         const float alpha = fast_exp2(m[k] - mx);
                         l[k] *= alpha;
@@ -493,20 +513,31 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                         for (int i = 0; i < CH * 8; ++i) acc[k][i] *= alpha;
                         m[k] = mx;
                     }
-                    const float p0 = fast_exp2(sc0 - m[k]);
-                    const float p1 = v1[k] ? fast_exp2(sc1 - m[k]) : 0.f;
-                    l[k] += p0 + p1;
+                    float pw[NPOS];
+#pragma unroll
+                    for (int n = 0; n < NPOS; ++n) {
+                        pw[n] = vv[k][n] ? fast_exp2(sc[n] - m[k]) : 0.f;
+                        l[k] += pw[n];
+                    }
 #pragma unroll
                     for (int i = 0; i < CH; ++i) {
-                        if (con[i]) {
+                        if (!CHK || con[i]) {
                             const int c8 = (lig + BDX * i) * 8;
-                            axpy8(&acc[k][i * 8], p0, *reinterpret_cast<const uint4 *>(sV + r0[k] + c8));
-                            if (v1[k])
-                                axpy8(&acc[k][i * 8], p1, *reinterpret_cast<const uint4 *>(sV + r1[k] + c8));
+#pragma unroll
+                            for (int n = 0; n < NPOS; ++n)
+                                if (vv[k][n])
+                                    axpy8(&acc[k][i * 8], pw[n],
+                                          *reinterpret_cast<const uint4 *>(sV + rr[k][n] + c8));
                         }
                     }
                 }
-            }
+            };
+            int t = 0;
+            // (t + NPOS) * phases <= np puts every slot's positions of the group
+            // inside the stage (ph < phases), and t + NPOS <= iters
+            if (all_con)
+                for (; (t + NPOS) * a.phases <= np; t += NPOS) group(t, std::false_type{});
+            for (; t < iters; t += NPOS) group(t, std::true_type{});
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[slot]);
         }
