@@ -14,10 +14,9 @@
 // chunk width from the expected number of pieces per unit: whole heads when
 // units have few pieces (many sequences), narrow chunks when one sequence is
 // spread over every partition, so each thread folds only a few pieces (the
-// merge itself is merge::merge_task, shared with the decode kernel's fused
-// merge).  Launched with
-// programmatic dependent launch: it may start while the decode kernel drains
-// and waits on griddepcontrol.wait before touching the workspace.
+// merge itself is merge::merge_task).  Launched with programmatic dependent
+// launch: it may start while the decode kernel drains and waits on
+// griddepcontrol.wait before touching the workspace.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -36,10 +35,11 @@ constexpr int kInlinePrefix = 4096;  // batches summed from current_pos in the c
 
 // INFLIGHT: piece loads each thread issues before folding them.  The host picks
 // the smallest depth that covers a thread's expected pieces in one round; the
-// shallow instances use few registers, so a whole batch's merge CTAs fit the
-// GPU in one wave.
+// shallow instances are bounded to 64 and 128 registers (8 and 4 CTAs per SM):
+// tighter bounds, which let more of a large batch's merge CTAs be resident at
+// once, spill and measured slower.
 template <int INFLIGHT>
-__global__ void __launch_bounds__(kThreads, INFLIGHT <= 2 ? 16 : (INFLIGHT <= 4 ? 8 : 1))
+__global__ void __launch_bounds__(kThreads, INFLIGHT <= 2 ? 8 : (INFLIGHT <= 4 ? 4 : 1))
     combine_kernel(const CombineArgs a) {
     __shared__ float sm_m[kThreads], sm_l[kThreads];
     __shared__ float4 sm_a[kThreads];

@@ -6,10 +6,13 @@
 // piece_slot(c_first + j, u).  The exact softmax-weighted sum over the unit's
 // whole live range is
 //   out = sum_j 2^(m_j - M) acc_j / sum_j 2^(m_j - M) l_j,   M = max_j m_j.
-// NT threads share one task: thread (sub, f) folds pieces sub, sub + nsub, ...
-// of float4 column f online, after issuing the loads of up to INFLIGHT of them
-// together; the per-thread states are then folded in two levels through shared
-// memory (groups of eight subs, then the group results).
+// NT threads share one task: thread (sub, f) takes pieces sub, sub + nsub, ...
+// of float4 column f, INFLIGHT of them per round with their loads issued
+// together; a round is absorbed with one rescale (its maximum first, then
+// independent weights).  The per-thread states are then merged across subs:
+// by an xor-shuffle butterfly inside each warp and one fold of the warps'
+// results when the column count divides 32, otherwise in two levels through
+// shared memory (groups of eight subs, then the group results).
 #pragma once
 
 #include <cuda_fp16.h>
@@ -47,6 +50,61 @@ __device__ __forceinline__ void fold(float &M, float &L, float4 &A, float m, flo
     A.y = fmaf(w, a.y, A.y);
     A.z = fmaf(w, a.z, A.z);
     A.w = fmaf(w, a.w, A.w);
+}
+
+// Merge state (m, l, a) into (M, L, A) symmetrically: both are rescaled to
+// the larger maximum.  Empty states (m = -inf, l = 0) contribute nothing.
+__device__ __forceinline__ void merge2(float &M, float &L, float4 &A, float m, float l, float4 a) {
+    const float nm = fmaxf(M, m);
+    if (nm == -INFINITY) return;  // both empty
+    const float s1 = ex2(M - nm), s2 = ex2(m - nm);  // ex2(-inf) = 0
+    L = fmaf(L, s1, l * s2);
+    A.x = fmaf(A.x, s1, a.x * s2);
+    A.y = fmaf(A.y, s1, a.y * s2);
+    A.z = fmaf(A.z, s1, a.z * s2);
+    A.w = fmaf(A.w, s1, a.w * s2);
+    M = nm;
+}
+
+// Absorb a round of N loaded pieces (empty ones have l = 0) into the running
+// state: the round's maximum first, then one rescale of the state and
+// independent weights 2^(m_r - M).
+template <int N>
+__device__ __forceinline__ void absorb(float &M, float &L, float4 &A, const float2 *ml,
+                                       const float4 *v) {
+    float mr = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < N; ++r)
+        if (ml[r].y > 0.f) mr = fmaxf(mr, ml[r].x);
+    if (mr == -INFINITY) return;  // nothing in this round
+    const float nm = fmaxf(M, mr);
+    const float s = ex2(M - nm);  // 0 while the state is empty
+    L *= s;
+    A.x *= s;
+    A.y *= s;
+    A.z *= s;
+    A.w *= s;
+#pragma unroll
+    for (int r = 0; r < N; ++r) {
+        const float w = ml[r].y > 0.f ? ex2(ml[r].x - nm) : 0.f;
+        L = fmaf(w, ml[r].y, L);
+        A.x = fmaf(w, v[r].x, A.x);
+        A.y = fmaf(w, v[r].y, A.y);
+        A.z = fmaf(w, v[r].z, A.z);
+        A.w = fmaf(w, v[r].w, A.w);
+    }
+    M = nm;
+}
+
+__device__ __forceinline__ void store_normalised(void *out, long long bh, int D, int col,
+                                                 float l, float4 A) {
+    const float inv = 1.f / l;
+    __half2 lo = __floats2half2_rn(A.x * inv, A.y * inv);
+    __half2 hi = __floats2half2_rn(A.z * inv, A.w * inv);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t *>(&lo);
+    packed.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(reinterpret_cast<__half *>(out) + bh * D + col) = packed;
 }
 
 __device__ __forceinline__ long long live_len(const uint32_t *cp, long long b, int S) {
@@ -93,9 +151,40 @@ __device__ __forceinline__ void merge_task(const float *ws_acc, const float2 *ws
                     v[r] = __ldcg(reinterpret_cast<const float4 *>(ws_acc + row * D + c0 + f * 4));
                 }
             }
-#pragma unroll
-            for (int r = 0; r < INFLIGHT; ++r) fold(M, L, A, ml[r].x, ml[r].y, v[r]);
+            absorb<INFLIGHT>(M, L, A, ml, v);
         }
+    }
+    if ((f4 & (f4 - 1)) == 0 && f4 <= 32) {
+        // nsub * f4 == NT: every thread holds a sub.  The subs of column f in
+        // one warp sit at lanes f, f + f4, ...: fold them with xor shuffles.
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            if (o < f4) break;
+            const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+            const float l2 = __shfl_xor_sync(0xffffffffu, L, o);
+            float4 a2;
+            a2.x = __shfl_xor_sync(0xffffffffu, A.x, o);
+            a2.y = __shfl_xor_sync(0xffffffffu, A.y, o);
+            a2.z = __shfl_xor_sync(0xffffffffu, A.z, o);
+            a2.w = __shfl_xor_sync(0xffffffffu, A.w, o);
+            merge2(M, L, A, m2, l2, a2);
+        }
+        const int warp = tid >> 5, lane = tid & 31;
+        if (lane < f4) {
+            sm_m[warp * f4 + lane] = M;
+            sm_l[warp * f4 + lane] = L;
+            sm_a[warp * f4 + lane] = A;
+        }
+        sync();
+        if (tid < f4) {
+            float m2 = sm_m[tid], l2 = sm_l[tid];
+            float4 a2 = sm_a[tid];
+#pragma unroll
+            for (int w = 1; w < NT / 32; ++w)
+                merge2(m2, l2, a2, sm_m[w * f4 + tid], sm_l[w * f4 + tid], sm_a[w * f4 + tid]);
+            store_normalised(out, bh, D, c0 + tid * 4, l2, a2);
+        }
+        return;
     }
     sm_m[tid] = M;
     sm_l[tid] = L;
@@ -127,14 +216,7 @@ __device__ __forceinline__ void merge_task(const float *ws_acc, const float2 *ws
             const int o = q * 8 * f4 + tid;
             fold(m2, l2, A2, sm_m[o], sm_l[o], sm_a[o]);
         }
-        const float inv = 1.f / l2;
-        __half2 lo = __floats2half2_rn(A2.x * inv, A2.y * inv);
-        __half2 hi = __floats2half2_rn(A2.z * inv, A2.w * inv);
-        uint2 packed;
-        packed.x = *reinterpret_cast<uint32_t *>(&lo);
-        packed.y = *reinterpret_cast<uint32_t *>(&hi);
-        *reinterpret_cast<uint2 *>(reinterpret_cast<__half *>(out) + bh * D + c0 + tid * 4) =
-            packed;
+        store_normalised(out, bh, D, c0 + tid * 4, l2, A2);
     }
 }
 
