@@ -52,7 +52,7 @@ constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
 #define DATTN_MIN_CONSUMER_WARPS 8  // 16: always sixteen consumer warps per CTA
 #endif
 #ifndef DATTN_PREFETCH_STAGES
-#define DATTN_PREFETCH_STAGES 3  // stages each CTA prefetches into L2 before its wait (0: none)
+#define DATTN_PREFETCH_STAGES 2  // stages each CTA prefetches into L2 before its wait (0: none)
 #endif
 #ifndef DATTN_MIN_HEAD_GROUPS
 #define DATTN_MIN_HEAD_GROUPS 1  // split the heads into at least this many groups

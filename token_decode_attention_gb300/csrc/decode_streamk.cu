@@ -177,6 +177,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         *abort_flag = 0;
         fence_barrier_init();
     }
+    __syncthreads();  // barrier initialisation visible to every warp
     // Launched with programmatic dependent launch: up to here only shared memory
     // is touched, so this CTA may already be resident while the kernel before it
     // on the stream finishes.  Everything after the wait sees that kernel's writes
@@ -209,57 +210,95 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     }
     pdl_wait_primary();
 
-    // ---- the CTA's range: block scan of the live lengths over the batch ----
-    const long long per = (a.B + kThreads - 1) / kThreads;
-    const long long bb = min(static_cast<long long>(threadIdx.x) * per, static_cast<long long>(a.B));
-    const long long be = min(bb + per, static_cast<long long>(a.B));
-    long long sum = 0;
-    for (long long b = bb; b < be; ++b) sum += live_len(a.cur_pos, b, a.S);
-    long long incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const long long y = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) s_warp_sum[warp] = incl;
-    __syncthreads();
-    long long before = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        const long long v = s_warp_sum[w];
-        if (w < warp) before += v;
-        total += v;
-    }
-    const long long excl = before + incl - sum;
+    // ---- the CTA's range: scan of the live lengths over the batch ----
+    // W = head_groups * sum_b L_b flattened positions cut into G ranges; this
+    // CTA owns [x0, x1), which starts in sequence b0 (at flattened position
+    // base0, live length L0).
     const long long nhg = a.head_groups;
-    const long long W = total * nhg;
     const unsigned G = static_cast<unsigned>(a.partitions);
-    const long long wq = W / G;
-    const unsigned wr = static_cast<unsigned>(W - wq * G);
-    const long long x0 = range_begin_split(blockIdx.x, wq, wr, G);
-    const long long x1 = range_begin_split(blockIdx.x + 1, wq, wr, G);
-    if (x0 < x1 && nhg * excl <= x0 && x0 < nhg * (excl + sum)) {
-        long long run = excl;
-        for (long long b = bb; b < be; ++b) {
-            const int L = live_len(a.cur_pos, b, a.S);
-            if (x0 < nhg * (run + L)) {
-                s_b0 = b;
-                s_base0 = nhg * run;
-                s_L0 = L;
-                break;
+    long long W, x0, x1, b0 = 0, base0 = 0;
+    int L0 = 0;
+    // range_begin_split needs W / G; a 32-bit division when W fits
+    auto cut = [&](long long total) {
+        W = total * nhg;
+        const long long wq = W < 0x100000000LL ? static_cast<long long>(static_cast<unsigned>(W) / G) : W / G;
+        const unsigned wr = static_cast<unsigned>(W - wq * G);
+        x0 = range_begin_split(blockIdx.x, wq, wr, G);
+        x1 = range_begin_split(blockIdx.x + 1, wq, wr, G);
+    };
+    if (a.B <= 32) {
+        // Lane b holds sequence b: every warp scans the batch on its own, with
+        // no shared memory and no CTA barrier.
+        const long long Lb = lane < a.B ? live_len(a.cur_pos, lane, a.S) : 0;
+        long long incl = Lb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        cut(__shfl_sync(kFull, incl, 31));
+        // the first sequence whose positions end past x0
+        const unsigned past = __ballot_sync(kFull, lane < a.B && x0 < nhg * incl);
+        if (past != 0u) {
+            const int first = __ffs(past) - 1;
+            L0 = static_cast<int>(__shfl_sync(kFull, Lb, first));
+            base0 = nhg * (__shfl_sync(kFull, incl, first) - L0);
+            b0 = first;
+        }
+        if (blockIdx.x == 0 && warp == 0 && a.ws_prefix != nullptr) {
+            if (lane < a.B) a.ws_prefix[lane] = incl - Lb;
+            if (lane == a.B - 1) a.ws_prefix[a.B] = incl;
+        }
+    } else {
+        // block scan: thread t sums sequences [bb, be)
+        const long long per = (a.B + kThreads - 1) / kThreads;
+        const long long bb = min(static_cast<long long>(threadIdx.x) * per, static_cast<long long>(a.B));
+        const long long be = min(bb + per, static_cast<long long>(a.B));
+        long long sum = 0;
+        for (long long b = bb; b < be; ++b) sum += live_len(a.cur_pos, b, a.S);
+        long long incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) s_warp_sum[warp] = incl;
+        __syncthreads();
+        long long before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const long long v = s_warp_sum[w];
+            if (w < warp) before += v;
+            total += v;
+        }
+        const long long excl = before + incl - sum;
+        cut(total);
+        if (x0 < x1 && nhg * excl <= x0 && x0 < nhg * (excl + sum)) {
+            long long run = excl;
+            for (long long b = bb; b < be; ++b) {
+                const int L = live_len(a.cur_pos, b, a.S);
+                if (x0 < nhg * (run + L)) {
+                    s_b0 = b;
+                    s_base0 = nhg * run;
+                    s_L0 = L;
+                    break;
+                }
+                run += L;
             }
-            run += L;
         }
-    }
-    if (blockIdx.x == 0 && a.ws_prefix != nullptr) {
-        long long run = excl;
-        for (long long b = bb; b < be; ++b) {
-            a.ws_prefix[b] = run;
-            run += live_len(a.cur_pos, b, a.S);
+        if (blockIdx.x == 0 && a.ws_prefix != nullptr) {
+            long long run = excl;
+            for (long long b = bb; b < be; ++b) {
+                a.ws_prefix[b] = run;
+                run += live_len(a.cur_pos, b, a.S);
+            }
+            if (threadIdx.x == 0) a.ws_prefix[a.B] = total;
         }
-        if (threadIdx.x == 0) a.ws_prefix[a.B] = total;
+        __syncthreads();
+        b0 = s_b0;
+        base0 = s_base0;
+        L0 = s_L0;
     }
-    __syncthreads();
     // The combine kernel may begin launching; it waits for this grid to finish.
     pdl_launch_dependents();
     if (x0 >= x1) return;  // empty range (fewer live positions than CTAs)
@@ -269,9 +308,9 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     Walker walk;
     walk.x = x0;
     walk.x1 = x1;
-    walk.b = s_b0;
-    walk.base = s_base0;
-    walk.Lb = s_L0;
+    walk.b = b0;
+    walk.base = base0;
+    walk.Lb = L0;
 
     __half *ring = reinterpret_cast<__half *>(smem);
     const size_t buf_elems = static_cast<size_t>(a.stage_pos) * a.heads_per_cta * D;
