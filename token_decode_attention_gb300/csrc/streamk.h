@@ -29,7 +29,10 @@ DATTN_HD long long range_begin(long long c, long long W, long long G) { return c
 // The partition whose range holds flattened position x (0 <= x < W): the
 // largest c with floor(c W / G) <= x, i.e. ceil((x + 1) G / W) - 1.
 DATTN_HD long long range_owner(long long x, long long W, long long G) {
-    return ((x + 1) * G + W - 1) / W - 1;
+    const long long n = (x + 1) * G + W - 1;
+    if (n < 0x100000000LL)  // a 32-bit division (W <= n)
+        return static_cast<long long>(static_cast<unsigned>(n) / static_cast<unsigned>(W)) - 1;
+    return n / W - 1;
 }
 
 // range_begin(c, W, G) with W = wq * G + wr (wq = W / G, wr = W % G) and
