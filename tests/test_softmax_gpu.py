@@ -130,3 +130,26 @@ def test_softmax_random_shapes(rows, cols, shifted, i):
     dattn.dattn_softmax_f32(x, out)
     torch.cuda.synchronize()
     check(x, out)
+
+
+def test_softmax_very_long_rows_with_masked_halves_and_nan():
+    # 160000 aligned columns (past 256 KB: one persistent 1024-thread CTA per
+    # SM, the row re-read from L2): a masked span across the middle, a whole
+    # half masked either side, a NaN in the second half only, and a single
+    # live entry in the first half.
+    g = torch.Generator(device="cuda").manual_seed(7)
+    x = torch.empty((5, 160000), dtype=torch.float32, device="cuda")
+    x.normal_(0.0, 3.0, generator=g)
+    x[0, 60000:100000] = float("-inf")     # across the split
+    x[1, 80000:] = float("-inf")           # the second half masked
+    x[2, 120000] = float("nan")            # a NaN in the second half only
+    x[3, :] = float("-inf")
+    x[3, 12345] = 2.0                      # one live entry, first half
+    x[4, :80000] = float("-inf")           # the first half masked
+    out = dattn.softmax(x)
+    torch.cuda.synchronize()
+    check(x, out)
+    assert (out[0, 60000:100000] == 0).all() and (out[1, 80000:] == 0).all()
+    assert torch.isnan(out[2]).all() and not torch.isnan(out[4]).any()
+    assert abs(float(out[3, 12345]) - 1.0) <= 1e-6 and float(out[3].abs().sum()) - float(out[3, 12345]) == 0.0
+    assert torch.allclose(out[[0, 1, 4]].double().sum(dim=1).cpu(), torch.ones(3, dtype=torch.float64), atol=1e-5)
