@@ -140,7 +140,7 @@ def test_softmax_very_long_rows_with_masked_halves_and_nan():
     g = torch.Generator(device="cuda").manual_seed(7)
     x = torch.empty((5, 160000), dtype=torch.float32, device="cuda")
     x.normal_(0.0, 3.0, generator=g)
-    x[0, 60000:100000] = float("-inf")     # across the split
+    x[0, 60000:100000] = float("-inf")     # across the middle
     x[1, 80000:] = float("-inf")           # the second half masked
     x[2, 120000] = float("nan")            # a NaN in the second half only
     x[3, :] = float("-inf")
