@@ -151,7 +151,6 @@ __global__ void __launch_bounds__(NT) softmax_reg_rows(const float *__restrict__
 // ---- long rows, persistent: one CTA per SM walks the rows, and the second
 // pass finds the row in L2 ----
 constexpr int kL2Threads = 1024;
-constexpr int kL2Unroll = 4;  // float4 loads in flight per thread
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -183,22 +182,25 @@ __global__ void __launch_bounds__(NT, kL2Threads / NT) softmax_l2_rows(const flo
     __shared__ int sm_nan[NT / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n4 = cols / 4;
+    // float4 loads in flight per thread: 6 fit the 512-thread instance's 64
+    // registers; the 1024-thread one spills beyond 4
+    constexpr int U = NT <= 512 ? 6 : 4;
     const uint64_t keep = l2_evict_last_policy();
     const uint64_t drop = l2_evict_first_policy();
     for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
         const float4 *x4 = reinterpret_cast<const float4 *>(x + r * cols);
         float m = -INFINITY, l = 0.f;
         bool nan = false;
-        for (int c = tid; c < n4; c += NT * kL2Unroll) {
-            float4 t[kL2Unroll];
+        for (int c = tid; c < n4; c += NT * U) {
+            float4 t[U];
 #pragma unroll
-            for (int k = 0; k < kL2Unroll; ++k) {
+            for (int k = 0; k < U; ++k) {
                 const int ck = c + k * NT;
                 t[k] = ck < n4 ? ld_f4_hint(x4 + ck, keep)
                                : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             }
 #pragma unroll
-            for (int k = 0; k < kL2Unroll; ++k) {
+            for (int k = 0; k < U; ++k) {
                 // m is kept in x units and S(m) = m log2(e) rounded once; a term is
                 // 2^(x log2(e) - S(m)) with the difference formed by one fused
                 // multiply-add, so S(m)'s rounding is common to every term and
@@ -243,15 +245,15 @@ __global__ void __launch_bounds__(NT, kL2Threads / NT) softmax_l2_rows(const flo
         const float inv = 1.f / l;
         const float sm = __fmul_rn(m, kLog2e);
         float4 *o4 = reinterpret_cast<float4 *>(out + r * cols);
-        for (int c = tid; c < n4; c += NT * kL2Unroll) {
-            float4 t[kL2Unroll];
+        for (int c = tid; c < n4; c += NT * U) {
+            float4 t[U];
 #pragma unroll
-            for (int k = 0; k < kL2Unroll; ++k) {
+            for (int k = 0; k < U; ++k) {
                 const int ck = c + k * NT;
                 if (ck < n4) t[k] = ld_f4_hint(x4 + ck, drop);
             }
 #pragma unroll
-            for (int k = 0; k < kL2Unroll; ++k) {
+            for (int k = 0; k < U; ++k) {
                 const int ck = c + k * NT;
                 if (ck < n4)
                     __stcs(o4 + ck, make_float4(ex2(fmaf(t[k].x, kLog2e, -sm)) * inv,
