@@ -190,6 +190,11 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     // warms L2, the point of coherence, so the reads after the wait still see
     // the final data.  Exact when the caches are full; elsewhere some of it is
     // read by other CTAs, the rest is wasted bandwidth.
+    //
+    // A paged cache finds its pages through the block table, which the previous
+    // kernel may still be writing: the entries read here are only used to pick
+    // what to prefetch, each checked to lie inside the page pool, and are read
+    // again after the wait for the copies.  A stale entry wastes a prefetch.
     if (threadIdx.x == 0 && a.prefetch_positions > 0) {
         const long long S = a.S;
         const long long Wc = static_cast<long long>(a.B) * S;  // capacity: the host keeps c * Wc in 64 bits
@@ -200,11 +205,23 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         while (x < x_end) {
             const long long b = x / S;
             const long long off = x - b * S;
-            const long long n = min(S - off, x_end - x);
-            const size_t first = static_cast<size_t>(b * S + off) * row;
-            const uint32_t bytes = static_cast<uint32_t>(n * row * 2);
-            bulk_prefetch_l2(reinterpret_cast<const __half *>(a.K) + first, bytes);
-            bulk_prefetch_l2(reinterpret_cast<const __half *>(a.V) + first, bytes);
+            long long n = min(S - off, x_end - x);
+            long long first_pos = b * S + off;  // dense: row index in [B*S]
+            bool go = true;
+            if (a.block_table != nullptr) {
+                const long long pidx = off / a.page_size;
+                const long long in_page = off - pidx * a.page_size;
+                n = min(n, static_cast<long long>(a.page_size) - in_page);
+                const long long page = a.block_table[b * a.max_pages + pidx];
+                go = page >= 0 && page < a.num_pages;
+                first_pos = page * a.page_size + in_page;
+            }
+            if (go) {
+                const size_t first = static_cast<size_t>(first_pos) * row;
+                const uint32_t bytes = static_cast<uint32_t>(n * row * 2);
+                bulk_prefetch_l2(reinterpret_cast<const __half *>(a.K) + first, bytes);
+                bulk_prefetch_l2(reinterpret_cast<const __half *>(a.V) + first, bytes);
+            }
             x += n;
         }
     }
