@@ -353,9 +353,9 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
     a.merge_offset = p.merge_offset;
     a.bar_offset = p.bar_offset;
     a.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
-    // one head group (dense or paged cache): prefetch the first stages into L2
-    // before the wait on the previous kernel
-    a.prefetch_positions = (DATTN_PREFETCH_STAGES > 0 && p.NHG == 1) ? DATTN_PREFETCH_STAGES * p.P : 0;
+    // dense or paged cache: prefetch the first stages into L2 before the wait on
+    // the previous kernel
+    a.prefetch_positions = DATTN_PREFETCH_STAGES > 0 ? DATTN_PREFETCH_STAGES * p.P : 0;
     cudaError_t e = dattn::launch_decode(a, p.v, p.smem, stream);
     if (e != cudaSuccess) return fail_cuda(e, "decode kernel launch");
     if (p.G > 1) {

@@ -61,8 +61,8 @@ struct DecodeArgs {
     int merge_offset;   // byte offset of the phase-merge area in dynamic smem
     int bar_offset;     // byte offset of the mbarriers in dynamic smem
     float qscale;       // log2(e) / sqrt(D), applied to each dot product
-    // One head group: positions of its first stages each CTA prefetches into L2
-    // before waiting on the kernel before it (0 = none).
+    // Positions of its first stages each CTA prefetches into L2 before waiting
+    // on the kernel before it (0 = none).
     int prefetch_positions;
 };
 

@@ -196,15 +196,19 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     // what to prefetch, each checked to lie inside the page pool, and are read
     // again after the wait for the copies.  A stale entry wastes a prefetch.
     if (threadIdx.x == 0 && a.prefetch_positions > 0) {
-        const long long S = a.S;
-        const long long Wc = static_cast<long long>(a.B) * S;  // capacity: the host keeps c * Wc in 64 bits
+        const long long S = a.S, nhg = a.head_groups;
+        // capacity (every sequence full): the host keeps c * Wc in 64 bits
+        const long long Wc = static_cast<long long>(a.B) * nhg * S;
         long long x = static_cast<long long>(blockIdx.x) * Wc / a.partitions;
         const long long x_end =
             min(x + a.prefetch_positions, static_cast<long long>(blockIdx.x + 1) * Wc / a.partitions);
         const size_t row = static_cast<size_t>(a.H) * a.D;  // halves per position
         while (x < x_end) {
-            const long long b = x / S;
-            const long long off = x - b * S;
+            const long long u = x / S;  // unit (b, g)
+            const long long off = x - u * S;
+            const long long b = u / nhg;
+            const int h0 = static_cast<int>(u - b * nhg) * a.heads_per_cta;
+            const int hg = min(a.heads_per_cta, a.H - h0);
             long long n = min(S - off, x_end - x);
             long long first_pos = b * S + off;  // dense: row index in [B*S]
             bool go = true;
@@ -217,10 +221,20 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                 first_pos = page * a.page_size + in_page;
             }
             if (go) {
-                const size_t first = static_cast<size_t>(first_pos) * row;
-                const uint32_t bytes = static_cast<uint32_t>(n * row * 2);
-                bulk_prefetch_l2(reinterpret_cast<const __half *>(a.K) + first, bytes);
-                bulk_prefetch_l2(reinterpret_cast<const __half *>(a.V) + first, bytes);
+                const __half *k0 = reinterpret_cast<const __half *>(a.K) + static_cast<size_t>(first_pos) * row;
+                const __half *v0 = reinterpret_cast<const __half *>(a.V) + static_cast<size_t>(first_pos) * row;
+                if (hg == a.H) {  // all heads: the run is one span
+                    const uint32_t bytes = static_cast<uint32_t>(n * row * 2);
+                    bulk_prefetch_l2(k0, bytes);
+                    bulk_prefetch_l2(v0, bytes);
+                } else {  // a head group: one span per position
+                    const uint32_t bytes = static_cast<uint32_t>(hg) * a.D * 2;
+                    for (long long j = 0; j < n; ++j) {
+                        const size_t o = static_cast<size_t>(j) * row + static_cast<size_t>(h0) * a.D;
+                        bulk_prefetch_l2(k0 + o, bytes);
+                        bulk_prefetch_l2(v0 + o, bytes);
+                    }
+                }
             }
             x += n;
         }
