@@ -63,12 +63,37 @@ DECODE_SOURCES = ("decode_streamk.cu", "combine.cu", "merge.cuh", "streamk.h", "
                   "dattn_internal.h", "dattn_api.cpp")
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments, trailing blanks and blank lines: what the
+    compiler sees, so that editing a comment keeps a recorded capture valid."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif text[i] == '"':  # string literal (PTX in asm statements): copied as is
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_source_hash() -> str:
+    """Hash of the decode path's sources (code only, comments stripped)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "token_decode_attention_gb300", "csrc")
     for name in DECODE_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -18,19 +18,23 @@
 // mask is a loop bound and masked rows are never read.
 //
 // Per CTA:
+//   * launched with programmatic dependent launch, it initialises its barriers
+//     and prefetches the first stages of its likely range into L2 before
+//     waiting on the kernel before it;
 //   * a producer warp streams, for each piece, stages of P positions: for the
 //     layout [B,S,H,D] the K rows of all heads of a run of positions are one
 //     contiguous span of HBM, moved by one bulk asynchronous copy
 //     (cp.async.bulk on the TMA engine, L2 evict-first) into a multi-stage
 //     shared-memory ring completing on mbarriers (V likewise);
-//   * eight consumer warps read each KV row with D/(8*CH) lanes, CH 16-byte
+//   * eight (or sixteen) consumer warps read each KV row with D/(8*CH) lanes, CH 16-byte
 //     shared loads per lane laid out so a lane group reads 128 contiguous
 //     bytes per load.  The QK product uses the raw f16 query and f16 keys with
 //     fp32 accumulation (products of two halves are exact in fp32); the dot is
 //     reduced with xor shuffles and scaled by log2(e)/sqrt(D).  Each lane group
 //     keeps an online softmax per (head, phase) slot in fp32 registers: the
 //     running max is only raised (and the state rescaled) when a new score
-//     exceeds it; PV accumulates with packed fp32x2 FMAs.
+//     exceeds it; PV accumulates with packed fp32x2 FMAs.  Groups of positions
+//     that lie wholly inside a stage run a body without per-position tests.
 //   * every mbarrier wait is bounded; a wait that runs out records an error in
 //     the device error word and the CTA returns after draining its copies.
 #include <cuda_fp16.h>
