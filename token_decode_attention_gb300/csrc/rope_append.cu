@@ -20,6 +20,7 @@
 #include <cmath>
 
 #include "dattn_internal.h"
+#include "ptx.cuh"
 
 namespace dattn {
 namespace {
@@ -117,6 +118,12 @@ __device__ __forceinline__ void store_rotated(__half *x, int i0, int i1, bool tr
 template <int VP>
 __global__ void __launch_bounds__(kThreads) rope_append_kernel(const RopeAppendArgs a) {
     __shared__ float cos_t[kRopeMaxPairs], sin_t[kRopeMaxPairs];
+    // Programmatic dependent launch on both sides: the kernel after this one
+    // (the decode) may start launching at once, since it reads nothing before
+    // waiting for this grid to complete; and this one reads nothing before the
+    // kernel before it has completed.
+    pdl_launch_dependents();
+    pdl_wait_primary();
     const int hpc = a.heads_per_cta;
     const int chunks = (a.H + hpc - 1) / hpc;
     const long long b = blockIdx.x / chunks;
@@ -215,8 +222,17 @@ cudaError_t launch_rope_append(const RopeAppendArgs &a, cudaStream_t stream) {
     void *args[] = {const_cast<RopeAppendArgs *>(&a)};
     const void *fn = a.rope_dims % 8 == 0 ? reinterpret_cast<const void *>(rope_append_kernel<4>)
                                           : reinterpret_cast<const void *>(rope_append_kernel<1>);
-    return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), args, 0,
-                            stream);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace dattn
