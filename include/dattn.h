@@ -169,9 +169,12 @@ int dattn_decode_f16(const void *Q, const void *K_cache, const void *V_cache, vo
  *
  * Each sequence's capacity is seq_len = page_size * max_pages (< 2^31).
  * Pages may be shared between sequences.  Entries for pages past a sequence's
- * live length are never read.  A live entry outside [0, num_pages) is not
- * dereferenced: page 0 is read instead, the output of that call is wrong, and
- * dattn_device_error() reports DATTN_ERR_BAD_PAGE.  The workspace is the one of
+ * live length have no effect: K and V are never read through them, and they
+ * raise no error.  (The kernel may read a few entries, live or not, as L2
+ * prefetch hints before the kernel before it on `stream` has finished; such a
+ * hint is bounds-checked and changes no result.)  A live entry outside
+ * [0, num_pages) is not dereferenced: page 0 is read instead, the output of
+ * that call is wrong, and dattn_device_error() reports DATTN_ERR_BAD_PAGE.  The workspace is the one of
  * dattn_decode_workspace_bytes(batch, n_heads, head_dim, page_size * max_pages,
  * num_partitions).
  * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA.
