@@ -80,7 +80,10 @@ def test_identity_table_equals_dense_decode_bit_for_bit():
     assert torch.equal(dense.view(torch.int16), paged.view(torch.int16))
 
 
-def test_unreferenced_pages_and_entries_past_live_length_are_never_read():
+def test_unreferenced_pages_and_entries_past_live_length_have_no_effect():
+    # K and V are never read through them (the producer may read such entries as
+    # bounds-checked L2 prefetch hints); NaN pages and invalid entries there
+    # leave the output bit-identical and raise no error
     B, H, D, ps, maxp = 3, 32, 128, 8, 10
     q, kp, vp, table = make_paged(5, B, H, D, ps, maxp, extra=6, share=False)
     cp = [30, 7, 55]  # live pages: 4, 1, 7
