@@ -81,7 +81,7 @@ def test_identity_table_equals_dense_decode_bit_for_bit():
 
 
 def test_unreferenced_pages_and_entries_past_live_length_have_no_effect():
-    # K and V are never read through them (the producer may read such entries as
+    # K and V are never read through them (the kernel may read such entries as
     # bounds-checked L2 prefetch hints); NaN pages and invalid entries there
     # leave the output bit-identical and raise no error
     B, H, D, ps, maxp = 3, 32, 128, 8, 10
