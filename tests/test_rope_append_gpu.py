@@ -208,3 +208,38 @@ def test_append_then_decode_is_one_decode_step():
         V_host[b, cp[b]] = to_np(vn[b])
     ref = oracle.decode_f64(q_ref, K_host, V_host, np.asarray(cp, np.uint32))
     assert_decode_close(out, ref, "rope + append + decode")
+
+
+def test_decode_steps_back_to_back_without_host_sync():
+    # rope/append and decode (with its merge) are launched with programmatic
+    # dependent launch: each kernel may begin launching before the one before it
+    # ends and waits for it before reading.  Several decode steps issued back to
+    # back on one stream, with every input staged beforehand and no host
+    # synchronisation in between, must each see the rows appended by its own and
+    # every earlier step.
+    g = torch.Generator(device="cuda").manual_seed(33)
+    B, H, D, S, steps = 2, 32, 128, 2048, 4
+    start = [1500, 700]
+    K, V = rand_f16(g, (B, S, H, D)), rand_f16(g, (B, S, H, D))
+    K_host, V_host = to_np(K).copy(), to_np(V).copy()
+    toks = [tuple(rand_f16(g, (B, H, D)) for _ in range(3)) for _ in range(steps)]
+    cps = [[s + t for s in start] for t in range(steps)]
+    cpts = [cur_pos_tensor(cp) for cp in cps]
+    q_rots = [torch.empty((B, H, D), dtype=torch.float16, device="cuda") for _ in range(steps)]
+    outs = [torch.empty((B, H, D), dtype=torch.float16, device="cuda") for _ in range(steps)]
+    torch.cuda.synchronize()
+    for t in range(steps):
+        q, kn, vn = toks[t]
+        dattn.rope_append(q, kn, vn, K, V, cpts[t], q_out=q_rots[t])
+        dattn.decode(q_rots[t], K, V, cpts[t], out=outs[t])
+    torch.cuda.synchronize()
+    for t in range(steps):
+        q, kn, vn = toks[t]
+        cp = cps[t]
+        k_ref = oracle.rope_f64(to_np(kn), cp).astype(np.float16)
+        for b in range(B):
+            K_host[b, cp[b]] = k_ref[b]
+            V_host[b, cp[b]] = to_np(vn[b])
+        q_ref = oracle.rope_f64(to_np(q), cp).astype(np.float16)
+        ref = oracle.decode_f64(q_ref, K_host, V_host, np.asarray(cp, np.uint32))
+        assert_decode_close(outs[t], ref, f"step {t}")
