@@ -1,6 +1,6 @@
 """Seeded random shapes, dense and paged, against the fp64 oracle.
 
-A hundred cases drawn from one seed: every head_dim class (multiples of 8 up
+Three hundred cases drawn from one seed: every head_dim class (multiples of 8 up
 to 256), head counts up to 80 (head groups included), ragged current_pos (some
 beyond seq_len), the library's partition count or a forced one (often more
 partitions than live positions, so some ranges are empty), and half of them
@@ -22,7 +22,7 @@ from ._util import assert_decode_close, cur_pos_tensor, rand_f16, to_np
 pytestmark = pytest.mark.gpu
 
 
-def draw_cases(n=100, seed=20260101):
+def draw_cases(n=300, seed=20260101):
     rng = np.random.default_rng(seed)
     cases = []
     while len(cases) < n:
