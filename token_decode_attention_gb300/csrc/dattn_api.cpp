@@ -170,13 +170,20 @@ std::map<PlanKey, Plan> g_plans;
 
 // Number of partitions (CTAs) when the caller leaves it to the library: every
 // resident CTA slot of the GPU, unless the batch's capacity is so small that a
-// partition would hold fewer than kMinPositions positions (then fewer CTAs, to
-// keep the partial states the combine must merge few).
+// partition would hold less than min_pos positions (then fewer CTAs, to keep
+// the partial states the combine must merge few).
 int choose_partitions(const Plan &p, int B, int S) {
     const long long slots = static_cast<long long>(p.sms) * p.ctas_per_sm;
     const long long capacity = static_cast<long long>(B) * p.NHG * S;
-    const long long min_pos = std::max<long long>(kMinPositions, 2LL * p.P);
-    const long long by_work = std::max<long long>(1, capacity / min_pos);
+    // At least a stage (and 8 positions) per partition when every head has its
+    // own lane group; with several phases per head a partition also pays a
+    // shared-memory merge per piece, so it keeps two stages (and
+    // kMinPositions).  Either way a small batch still spreads over up to 32
+    // partitions of a stage each.
+    const long long min_pos = p.PHI == 1 ? std::max<long long>(8, p.P)
+                                         : std::max<long long>(kMinPositions, 2LL * p.P);
+    const long long by_work =
+        std::max<long long>({1, capacity / min_pos, std::min<long long>(32, capacity / p.P)});
     return static_cast<int>(std::min<long long>({slots, by_work, kMaxPartitions}));
 }
 
