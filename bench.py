@@ -1,8 +1,9 @@
 """Benchmark: decode-attention effective HBM GB/s and query-heads/s on GB300.
 
 One step = one fused decode call (split-K kernel + combine) over one batch of
-synthetic input of the chosen workload (default: the 7B-class decode step,
-B=1 H=32 D=128 S=4096 current_pos=4095).  Prints ONE JSON line.
+synthetic input of the chosen workload (default: the largest one that fits one
+GPU, the large-batch workload B=256 H=40 D=128 S=8192 current_pos=8191 with
+outlier key channels, 40 GiB of K+V).  Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl ours|reference] [--no-sweep] [--cpu-seconds T]
@@ -16,7 +17,8 @@ previous one.  N > 1 runs one independent replica per GPU (weak scaling): the
 path shards by sequence with no data exchange.
 
 --impl reference times the CPU oracle (the plain fp64 restatement of the
-method) on this host's cores, on the same workload, metric and unit.
+method) on this host's cores, on the same workload, metric and unit; each step
+is one pass over a bounded sample of the workload's sequences (same recipe).
 """
 from __future__ import annotations
 
@@ -41,6 +43,43 @@ from token_decode_attention_gb300.workloads import (  # noqa: E402
 METRIC = "decode-attention effective HBM GB/s (% of GB300 peak) and query-heads/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+GB300_L2_BYTES = 129 * 2**20  # used when no device is visible
+# Sequences of a workload the CPU oracle takes per pass when the whole workload
+# would take it more than a few seconds (the oracle streams ~6 GB/s): 16 of the
+# outlier workload's 256 sequences are 2.7 GB.
+CPU_SAMPLE_SEQUENCES = {"outlier": 16}
+
+
+def input_sets(kv_bytes: int, l2_bytes: int) -> int:
+    """Independent input sets a step rotates through so that no step reads inputs
+    left in L2 by the previous one: one when K+V alone exceed 4x L2."""
+    return 1 if kv_bytes >= 4 * l2_bytes else min(4096, math.ceil(4 * l2_bytes / kv_bytes) + 1)
+
+
+def l2_note(kv_bytes: int, l2_bytes: int) -> str:
+    n = input_sets(kv_bytes, l2_bytes)
+    if n == 1:
+        return f"inputs larger than L2 ({kv_bytes / 2**30:.2f} GiB K+V)"
+    return f"rotating {n} input sets, {n * kv_bytes / 2**30:.2f} GiB K+V in total (> 4x L2)"
+
+
+def workload_config(w, world: int, l2_bytes: int) -> dict:
+    """The `config` object of the JSON line: the workload only, identical for
+    both arms (the kernel plan is reported beside it)."""
+    return {"workload": f"{w.name}: {w.description}", "batch": w.batch,
+            "n_heads": w.n_heads, "head_dim": w.head_dim, "seq_len": w.seq_len,
+            "current_pos": "per-sequence" if w.current_pos is None else w.current_pos,
+            "l2": l2_note(w.kv_bytes(), l2_bytes), "parallelism": f"replicas x{world}"}
+
+
+def device_l2_bytes() -> int:
+    try:
+        if torch.cuda.is_available():
+            props = torch.cuda.get_device_properties(torch.cuda.current_device())
+            return int(getattr(props, "L2_cache_size", 0) or GB300_L2_BYTES)
+    except Exception:
+        pass
+    return GB300_L2_BYTES
 
 
 def log(*a):
@@ -247,7 +286,7 @@ class Replica:
                                              description=w.description + f", batch {batch}")
         self.device = device
         kv = w.kv_bytes()
-        self.sets_n = 1 if kv >= 4 * l2_bytes else min(4096, math.ceil(4 * l2_bytes / kv) + 1)
+        self.sets_n = input_sets(kv, l2_bytes)
         base = make_inputs(WORKLOADS[name], device, batch=w.batch)
         self.cp_host = base["cur_pos_host"]
         self.page_size = page_size
@@ -271,9 +310,7 @@ class Replica:
         # stream.  Finish it here so no buffer freed by the set-up (and reused
         # by the allocator) is still being read when the side stream writes.
         torch.cuda.synchronize(device)
-        self.l2_note = (f"inputs larger than L2 ({kv / 2**30:.2f} GiB K+V)" if self.sets_n == 1
-                        else f"rotating {self.sets_n} input sets, {self.sets_n * kv / 2**30:.2f}"
-                             f" GiB K+V in total (> 4x L2)")
+        self.l2_note = l2_note(kv, l2_bytes)
 
     def step(self, i: int, stream):
         x = self.sets[i % self.sets_n]
@@ -460,8 +497,7 @@ class Replica:
                         "current_pos (dattn_rope_append_f16), decode, out copied D2H into "
                         "pinned memory; 'eager' issues the same calls from Python each step; "
                         "the KV cache is device-resident state; value counts the decode's "
-                        "bytes only; the median of three timing windows (the step settles "
-                        "at ~27 or ~36 us per window)"}
+                        "bytes only; the median of three timing windows"}
 
 
 def graph_time_us(fn, steps: int, warmup: int, stream, graph: bool = True) -> float:
@@ -564,7 +600,8 @@ def sweep_ops(device, stream, steps: int, warmup: int, peak: float, only: str | 
     return res
 
 
-def cpu_baseline(name: str, budget_s: float, max_reps: int = 1000, batch: int = 0) -> dict:
+def cpu_baseline(name: str, budget_s: float, max_reps: int = 1000, batch: int = 0,
+                 device: str = "cuda") -> dict:
     """The CPU oracle, as it stands, on a bounded sample of the workload
     (`batch` > 0: that many sequences of the same recipe)."""
     import oracle
@@ -572,7 +609,7 @@ def cpu_baseline(name: str, budget_s: float, max_reps: int = 1000, batch: int = 
     if batch:
         import dataclasses
         w = dataclasses.replace(w, batch=batch)
-    x = make_inputs(WORKLOADS[name], "cuda", batch=w.batch)
+    x = make_inputs(WORKLOADS[name], device, batch=w.batch)
     q, k, v = (x[n].cpu().numpy() for n in ("q", "k", "v"))
     cp = x["cur_pos_host"]
     del x
@@ -598,7 +635,7 @@ def cpu_sweep(budget_s: float) -> dict:
     res = {}
     for name in ("small", "7b", "ragged", "long", "outlier"):
         try:
-            r = cpu_baseline(name, budget_s, batch=16 if name == "outlier" else 0)
+            r = cpu_baseline(name, budget_s, batch=CPU_SAMPLE_SEQUENCES.get(name, 0))
             res[name] = {k: r[k] for k in ("value", "unit", "query_heads_per_s", "seconds",
                                            "cores", "sample")}
         except Exception as e:
@@ -637,14 +674,23 @@ def sweep(device, stream, l2_bytes: int, steps: int, warmup: int, peak: float) -
 # ---------------------------------------------------------------- main
 
 def run_reference(args, world, rank):
+    """The oracle, as it stands, on this host's cores: each step one pass over
+    the workload, or over a bounded sample of its sequences (same recipe)
+    where the whole workload would take minutes."""
     if rank != 0:
         return
+    import dataclasses
+
     import oracle
-    w = WORKLOADS[args.workload]
-    # the oracle's inputs: same shapes and recipe, drawn on the host
-    x = make_inputs(w, "cpu")
-    q, k, v = (x[n].numpy() for n in ("q", "k", "v"))
+    full = WORKLOADS[args.workload]
+    sample = CPU_SAMPLE_SEQUENCES.get(full.name, 0)
+    w = dataclasses.replace(full, batch=sample) if sample else full
+    # drawn on the GPU when there is one (the host's float16 sampler is
+    # single-threaded: ~1 min for this sample), then copied to the host
+    x = make_inputs(full, "cuda" if torch.cuda.is_available() else "cpu", batch=w.batch)
+    q, k, v = (x[n].cpu().numpy() for n in ("q", "k", "v"))
     cp = x["cur_pos_host"]
+    del x
     nbytes = algorithmic_bytes(w.batch, w.n_heads, w.head_dim, w.seq_len, cp)
     for _ in range(args.warmup):
         oracle.decode_f64(q, k, v, cp)
@@ -653,17 +699,17 @@ def run_reference(args, world, rank):
         oracle.decode_f64(q, k, v, cp)
     el = time.perf_counter() - t0
     val = nbytes * args.steps / el / 1e9
+    what = (f"each step one pass over {sample} of the {full.batch} sequences of the {full.name} "
+            f"workload (same recipe)" if sample else
+            f"each step one full pass of the {full.name} workload")
     line = {"metric": METRIC, "value": val, "unit": "GB/s", "impl": "reference",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{w.name}: {w.description}", "batch": w.batch,
-                       "n_heads": w.n_heads, "head_dim": w.head_dim, "seq_len": w.seq_len,
-                       "parallelism": "replicas"},
+            "config": workload_config(full, world, device_l2_bytes()),
             "query_heads_per_s": w.batch * w.n_heads * args.steps / el,
             "cpu_baseline": {"value": val, "unit": "GB/s", "cores": oracle.max_threads(),
-                             "kind": "oracle",
-                             "sample": f"each step one full pass of the {w.name} workload"},
+                             "kind": "oracle", "sample": what + ", fp64 C oracle with OpenMP"},
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -674,7 +720,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="7b", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="outlier", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--eager", action="store_true",
@@ -759,11 +805,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
-        "config": {"workload": f"{w.name}: {w.description}", "batch": w.batch,
-                   "n_heads": w.n_heads, "head_dim": w.head_dim, "seq_len": w.seq_len,
-                   "current_pos": "per-sequence" if w.current_pos is None else w.current_pos,
-                   "partitions": rep.plan["partitions"], "l2": rep.l2_note,
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(w, world, l2),
         "query_heads_per_s": job["query_heads_per_s"],
         "frac_of_nominal_8TBs": per_call / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": per_call, "peak": peak, "unit": "GB/s",
@@ -784,7 +826,8 @@ def main():
     del rep
     torch.cuda.empty_cache()
     if world == 1:
-        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds,
+                                            batch=CPU_SAMPLE_SEQUENCES.get(args.workload, 0))
         if not args.no_sweep:
             line["sweep"] = sweep(device, stream, l2, 20, 3, peak)
             line["sweep_ops"] = sweep_ops(device, stream, 20, 3, peak)

@@ -32,6 +32,17 @@
  *     `pos > current_pos` never fires then: the live length is
  *     L = min(current_pos, seq_len - 1) + 1.  The library never reads
  *     current_pos on the host.
+ *   - Errors found while a kernel runs (a pipeline wait that ran out, a bad
+ *     block-table entry, an append position outside the cache) cannot change a
+ *     return value that was already given: the kernel records them in a device
+ *     error word instead, and the outputs of the affected call are not valid.
+ *     dattn_device_error() synchronises the device and reports that word; a
+ *     caller that must know an output is valid checks it after the call.
+ *   - The library keeps per-device state for the life of the process: kernel
+ *     attributes, the address of the device error word, plans and the
+ *     no-alloc scratch address.  cudaDeviceReset() (or any other teardown of the
+ *     device's primary context) invalidates it; do not reset a device while the
+ *     library is in use on it.
  */
 #ifndef DATTN_H
 #define DATTN_H
@@ -134,6 +145,10 @@ int dattn_decode_workspace_bytes(int batch, int n_heads, int head_dim, int seq_l
  * (log-sum-exp merge); both are enqueued on `stream`.
  *
  * Concurrent calls on different streams need different workspaces.
+ * A return of DATTN_OK means the kernels were enqueued.  The output is valid
+ * once the stream has reached them and dattn_device_error() reports DATTN_OK:
+ * a CTA whose bounded pipeline wait ran out (after one second) leaves its part
+ * of `out` unwritten and records DATTN_ERR_TIMEOUT in the device error word.
  * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA.
  */
 int dattn_decode_f16_ex(const void *Q, const void *K_cache, const void *V_cache, void *out,

@@ -252,20 +252,24 @@ def test_workload_long_context_full_parity():
 
 
 @pytest.mark.slow
-def test_workload_outlier_sampled_parity():
-    # full 40 GiB workload in the launch configuration the benchmark uses; the
-    # oracle checks a seeded sample of 16 sequences x all 40 heads
+def test_workload_outlier_full_parity():
+    # The whole 40 GiB workload (256 sequences x 40 heads) in the launch
+    # configuration the benchmark uses, every output element against the fp64
+    # oracle.  The inputs stay on the device; the oracle takes them a few
+    # sequences at a time, so the host holds ~1.3 GB at once.
     w = WORKLOADS["outlier"]
     x = make_inputs(w, "cuda")
     out = dattn.decode(x["q"], x["k"], x["v"], x["cur_pos"])
     torch.cuda.synchronize()
-    rng = np.random.default_rng(w.seed)
-    sample = np.sort(rng.choice(w.batch, size=16, replace=False))
-    for b in sample:
-        sl = slice(int(b), int(b) + 1)
-        ref = oracle.decode_f64(to_np(x["q"][sl]), to_np(x["k"][sl]), to_np(x["v"][sl]),
+    got = to_np(out)
+    q = to_np(x["q"])
+    step = 8
+    for b0 in range(0, w.batch, step):
+        sl = slice(b0, min(w.batch, b0 + step))
+        ref = oracle.decode_f64(q[sl], to_np(x["k"][sl]), to_np(x["v"][sl]),
                                 x["cur_pos_host"][sl])
-        assert_decode_close(out[sl], ref, f"{w.description}, sequence {b}")
+        assert_decode_close(torch.from_numpy(got[sl]), ref,
+                            f"{w.description}, sequences {sl.start}..{sl.stop - 1}")
     del x
     torch.cuda.empty_cache()
 

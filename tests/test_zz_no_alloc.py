@@ -4,9 +4,14 @@ Callers such as runtimes that own all device memory through their own pool, or
 code running where a cudaMalloc is forbidden or would synchronise the device,
 cannot hand the library a freshly allocated workspace.  This entry point uses a
 static device array built into the library instead.  Here it is called
-through the C ABI (ctypes, raw device pointers) and its output is compared with
-the workspace-taking entry point dattn_decode_f16_ex on the same inputs, on two
-calls in a row, within the decode tolerance of the other tests.
+through the C ABI (ctypes, raw device pointers).  It runs the same plan and the
+same kernels as the workspace-taking entry point dattn_decode_f16_ex with the
+library-chosen partition count, so its output must be bit-identical to that
+call's on the same inputs: that is checked on calls made back to back, among
+them two calls of one shape on different inputs (the second finds the first
+one's partial states left in the scratch and must not be affected by them).
+One output is also compared with the fp64 oracle within the decode tolerance
+of the other tests.
 
 This file is named so that pytest collects it last; it passes alone in a fresh
 process as well as after the other tests.
@@ -17,9 +22,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from token_decode_attention_gb300 import _native, build
 
-from ._util import ATOL, RTOL, cur_pos_tensor, rand_f16
+from ._util import assert_decode_close, cur_pos_tensor, rand_f16, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +47,8 @@ def _noalloc(lib, q, k, v, out, cp):
 
 
 def _reference(q, k, v, cp):
-    """The existing entry point, with a workspace allocated by the test."""
+    """The existing entry point, with a workspace allocated by the test and the
+    library-chosen partition count (the plan the no-alloc call uses)."""
     B, H, D = q.shape
     S = k.shape[1]
     out = torch.empty((B, H, D), dtype=torch.float16, device="cuda")
@@ -51,30 +58,32 @@ def _reference(q, k, v, cp):
     return out
 
 
-def _close(got, ref, what):
-    g = got.double().cpu().numpy()
-    r = ref.double().cpu().numpy()
-    err = np.abs(g - r)
-    assert (err <= ATOL + RTOL * np.abs(r)).all(), f"{what}: max err {err.max():.3g}"
+def _inputs(g, B, H, D, S):
+    return rand_f16(g, (B, H, D)), rand_f16(g, (B, S, H, D)), rand_f16(g, (B, S, H, D))
 
 
-def test_two_calls_in_a_row_match_the_workspace_entry_point(lib):
+def test_calls_in_a_row_match_the_workspace_entry_point_bit_for_bit(lib):
     g = torch.Generator(device="cuda").manual_seed(20260123)
     cases = [
-        # (B, H, D, S, current_pos): both need split-K scratch
+        # (B, H, D, S, current_pos): all need split-K scratch.  The first two
+        # are one shape on different inputs and current_pos.
         (1, 32, 128, 4096, [4095]),
+        (1, 32, 128, 4096, [1777]),
         (6, 8, 64, 1500, [1499, 0, 700, 3, 1200, 999]),
     ]
     for i, (B, H, D, S, cp) in enumerate(cases):
         assert _native.dattn_decode_workspace_bytes(B, H, D, S, 0) > 0
-        q, k, v = rand_f16(g, (B, H, D)), rand_f16(g, (B, S, H, D)), rand_f16(g, (B, S, H, D))
+        q, k, v = _inputs(g, B, H, D, S)
         cpt = cur_pos_tensor(cp)
         out = torch.full((B, H, D), float("nan"), dtype=torch.float16, device="cuda")
         st = _noalloc(lib, q, k, v, out, cpt)
         assert st == 0, lib.dattn_last_error().decode()
         ref = _reference(q, k, v, cpt)
         torch.cuda.synchronize()
-        _close(out, ref, f"call {i + 1}")
+        assert torch.equal(out, ref), f"call {i + 1}: differs from dattn_decode_f16_ex"
+        if i == 0:
+            exact = oracle.decode_f64(to_np(q), to_np(k), to_np(v), np.asarray(cp, np.uint32))
+            assert_decode_close(out, exact, f"call {i + 1} against the oracle")
     assert _native.dattn_device_error(clear=True) == 0
 
 

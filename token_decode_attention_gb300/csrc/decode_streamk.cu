@@ -220,7 +220,8 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                 const long long pidx = off / a.page_size;
                 const long long in_page = off - pidx * a.page_size;
                 n = min(n, static_cast<long long>(a.page_size) - in_page);
-                const long long page = a.block_table[b * a.max_pages + pidx];
+                // through L2 only (no L1 line is left behind for the reads after the wait)
+                const long long page = __ldcg(a.block_table + b * a.max_pages + pidx);
                 go = page >= 0 && page < a.num_pages;
                 first_pos = page * a.page_size + in_page;
             }
@@ -415,7 +416,9 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                         const int off = pos - pidx * a.page_size;
                         if (page_first < 0 || pidx < page_first || pidx >= page_first + 32) {
                             page_first = pidx;
-                            page_lane = (pidx + lane < a.max_pages) ? __ldg(bt + pidx + lane) : 0;
+                            // coherent load: the table may have been written by the
+                            // kernel before this one, after the pre-wait prefetch read it
+                            page_lane = (pidx + lane < a.max_pages) ? __ldcg(bt + pidx + lane) : 0;
                         }
                         long long page = __shfl_sync(kFull, page_lane, pidx - page_first);
                         if (page < 0 || page >= a.num_pages) {  // never read outside the pages
