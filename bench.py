@@ -301,11 +301,15 @@ class Replica:
         self.partitions = partitions
         self.plan = dattn.dattn_decode_plan(w.batch, w.n_heads, w.head_dim, w.seq_len,
                                             partitions)
-        nbytes = max(16, self.plan["workspace_bytes"])
+        # enough for the dense and the paged call of this shape
+        nbytes = max(16, dattn.dattn_decode_workspace_bytes(w.batch, w.n_heads, w.head_dim,
+                                                            w.seq_len, partitions))
         self.ws = torch.empty((nbytes,), dtype=torch.uint8, device=device)
         self.bytes_per_step = algorithmic_bytes(w.batch, w.n_heads, w.head_dim, w.seq_len,
                                                 self.cp_host)
-        self.launches_per_step = 1 + (1 if self.plan["partitions"] > 1 else 0)
+        # the decode kernel, plus the merge kernel of a split plan
+        self.launches_per_step = 1 + (1 if self.plan["partitions"] > 1 and
+                                      self.plan["cluster_size"] == 0 else 0)
         # Everything above ran on the default stream; the steps run on a side
         # stream.  Finish it here so no buffer freed by the set-up (and reused
         # by the allocator) is still being read when the side stream writes.

@@ -83,11 +83,16 @@ const char *dattn_last_error(void);
  * Execution plan of the fused decode for a shape on the current device.
  * Filled by dattn_decode_plan(); informational.
  *
- * The decode is "stream-K": the live positions of the whole batch, flattened
- * over (sequence, head group, position), are cut into `partitions` equal
- * ranges, one per CTA, so every CTA streams the same number of KV bytes
- * whatever the mix of sequence lengths.  A sequence whose positions span
- * several ranges is finished by a merge kernel.
+ * Two plans exist.  The split plan ("stream-K"): the live positions of the
+ * whole batch, flattened over (sequence, head group, position), are cut into
+ * `partitions` equal ranges, one per CTA, so every CTA streams the same number
+ * of KV bytes whatever the mix of sequence lengths; a sequence whose positions
+ * span several ranges is finished by a merge kernel.  The cluster plan (a
+ * dense cache of a single sequence, library-chosen partitions): one
+ * thread-block cluster of `cluster_size` CTAs per (sequence, head group); the
+ * CTAs of a cluster split the live positions and merge their partial softmax
+ * states through distributed shared memory, so one launch writes `out` and no
+ * workspace is used.
  */
 typedef struct dattn_plan {
     int partitions;      /* CTAs of the decode grid (equal ranges of positions)  */
@@ -100,6 +105,8 @@ typedef struct dattn_plan {
     int ctas_per_sm;     /* resident CTAs per SM at that shared-memory size      */
     int sm_count;
     size_t workspace_bytes;
+    int cluster_size;    /* > 0: cluster plan, CTAs per cluster (no workspace,   */
+                         /* no merge kernel); 0: stream-K over the batch          */
 } dattn_plan;
 
 /*
@@ -113,11 +120,13 @@ int dattn_decode_plan(int batch, int n_heads, int head_dim, int seq_len, int num
                       dattn_plan *plan);
 
 /*
- * Workspace that dattn_decode_f16_ex needs for this shape and num_partitions
- * on the current device, in bytes (0 when there is a single partition).  It
- * holds the batch's live-length prefix sums and one fp32 partial softmax state
- * (m, l, acc[head_dim]) per head for each (partition, head group) piece; it is
- * scratch, rewritten by every call.
+ * Workspace that dattn_decode_f16_ex and dattn_decode_paged_f16 need for this
+ * shape and num_partitions on the current device, in bytes: the larger of the
+ * two calls' needs (0 when the split plan has a single partition; the cluster
+ * plan of a dense cache needs none, dattn_decode_plan() reports the dense
+ * call's own figure).  It holds the batch's live-length prefix sums and one
+ * fp32 partial softmax state (m, l, acc[head_dim]) per head for each
+ * (partition, head group) piece; it is scratch, rewritten by every call.
  * Errors: as dattn_decode_plan, plus INVALID_ARG for a null `bytes`.
  */
 int dattn_decode_workspace_bytes(int batch, int n_heads, int head_dim, int seq_len,
@@ -140,9 +149,10 @@ int dattn_decode_workspace_bytes(int batch, int n_heads, int head_dim, int seq_l
  * computed with fp32 accumulation and an online (running max/sum) softmax, then
  * rounded to f16 (round to nearest even).  Positions p >= L are never read: the
  * page's -infinity score gives them weight exactly zero.  The live positions are
- * divided into equal ranges across CTAs (see dattn_plan); the partial softmax
- * states of a sequence that spans several ranges are merged by a second kernel
- * (log-sum-exp merge); both are enqueued on `stream`.
+ * divided among CTAs (see dattn_plan); the partial softmax states of a
+ * sequence that spans several CTAs are merged (log-sum-exp merge) by a second
+ * kernel, or, in the cluster plan, through distributed shared memory within
+ * the same launch.  Everything is enqueued on `stream`.
  *
  * Concurrent calls on different streams need different workspaces.
  * A return of DATTN_OK means the kernels were enqueued.  The output is valid

@@ -85,10 +85,13 @@ def test_recorded_decodes_replay_on_new_contents():
 
 def test_growing_the_library_workspace_while_recording_is_refused_cleanly():
     g = torch.Generator(device="cuda").manual_seed(9)
-    B, H, D, S = 1, 32, 128, 5000
+    # two sequences: the split plan, which needs a workspace (a single
+    # sequence would take the cluster plan, which needs none)
+    B, H, D, S = 2, 32, 128, 5000
+    assert dattn.dattn_decode_plan(B, H, D, S)["workspace_bytes"] > 0
     q, k, v = rand_f16(g, (B, H, D)), rand_f16(g, (B, S, H, D)), rand_f16(g, (B, S, H, D))
     out = torch.empty_like(q)
-    cp = cur_pos_tensor([4999])  # made before recording: no copies while recording
+    cp = cur_pos_tensor([4999, 1234])  # made before recording: no copies while recording
     s = torch.cuda.Stream()  # a fresh stream: its library workspace does not exist yet
     s.wait_stream(torch.cuda.current_stream())
     torch.cuda.synchronize()
@@ -103,7 +106,7 @@ def test_growing_the_library_workspace_while_recording_is_refused_cleanly():
     # outside recording the same call works
     dattn.dattn_decode_f16(q, k, v, out, cp, s)
     torch.cuda.synchronize()
-    ref = oracle.decode_f64(to_np(q), to_np(k), to_np(v), np.array([4999], np.uint32))
+    ref = oracle.decode_f64(to_np(q), to_np(k), to_np(v), np.array([4999, 1234], np.uint32))
     assert_decode_close(out, ref, "after the refused recording")
 
 

@@ -65,14 +65,16 @@ def _inputs(g, B, H, D, S):
 def test_calls_in_a_row_match_the_workspace_entry_point_bit_for_bit(lib):
     g = torch.Generator(device="cuda").manual_seed(20260123)
     cases = [
-        # (B, H, D, S, current_pos): all need split-K scratch.  The first two
-        # are one shape on different inputs and current_pos.
-        (1, 32, 128, 4096, [4095]),
-        (1, 32, 128, 4096, [1777]),
+        # (B, H, D, S, current_pos): all take the split plan, whose partial
+        # states go through the scratch.  The first two are one shape on
+        # different inputs and current_pos.
+        (2, 32, 128, 4096, [4095, 1000]),
+        (2, 32, 128, 4096, [1777, 4095]),
         (6, 8, 64, 1500, [1499, 0, 700, 3, 1200, 999]),
     ]
     for i, (B, H, D, S, cp) in enumerate(cases):
-        assert _native.dattn_decode_workspace_bytes(B, H, D, S, 0) > 0
+        plan = _native.dattn_decode_plan(B, H, D, S, 0)
+        assert plan["cluster_size"] == 0 and plan["workspace_bytes"] > 0
         q, k, v = _inputs(g, B, H, D, S)
         cpt = cur_pos_tensor(cp)
         out = torch.full((B, H, D), float("nan"), dtype=torch.float16, device="cuda")

@@ -31,7 +31,8 @@ class Plan(ctypes.Structure):
                 ("head_groups", ctypes.c_int), ("stage_positions", ctypes.c_int),
                 ("stages", ctypes.c_int), ("threads_per_cta", ctypes.c_int),
                 ("smem_bytes", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
-                ("sm_count", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
+                ("sm_count", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
+                ("cluster_size", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

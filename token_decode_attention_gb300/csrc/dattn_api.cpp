@@ -7,6 +7,8 @@
 // kernels (decode_streamk.cu, combine.cu, split_calls.cu).
 #include "dattn.h"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -54,12 +56,42 @@ constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
 #ifndef DATTN_PREFETCH_STAGES
 #define DATTN_PREFETCH_STAGES 2  // stages each CTA prefetches into L2 before its wait (0: none)
 #endif
+#ifndef DATTN_PREFETCH_THREADS
+#define DATTN_PREFETCH_THREADS 0  // 1: every thread prefetches lines; 0: bulk prefetches (TMA)
+#endif
 #ifndef DATTN_MIN_HEAD_GROUPS
 #define DATTN_MIN_HEAD_GROUPS 1  // split the heads into at least this many groups
 #endif
 #ifndef DATTN_MIN_POSITIONS
 #define DATTN_MIN_POSITIONS 16
 #endif
+// Cluster mode (one cluster of CTAs per (sequence, head group), merged in
+// distributed shared memory; see DecodeArgs::cluster).
+#ifndef DATTN_CLUSTER_MAX_BATCH
+#define DATTN_CLUSTER_MAX_BATCH 1  // sequences up to which cluster mode is considered
+#endif
+#ifndef DATTN_CLUSTER_STAGE_BYTES
+#define DATTN_CLUSTER_STAGE_BYTES (64 * 1024)  // K+V per pipeline stage
+#endif
+#ifndef DATTN_CLUSTER_MIN_CTA_BYTES
+#define DATTN_CLUSTER_MIN_CTA_BYTES (32 * 1024)  // K+V capacity per CTA at least
+#endif
+#ifndef DATTN_CLUSTER_MAX_CAPACITY_BYTES
+#define DATTN_CLUSTER_MAX_CAPACITY_BYTES (512LL << 20)  // K+V capacity up to which it is used
+#endif
+#ifndef DATTN_CLUSTER_MAX_SIZE
+#define DATTN_CLUSTER_MAX_SIZE 16  // CTAs per cluster (8 is the portable limit)
+#endif
+#ifndef DATTN_CLUSTER_PREFER_SMALL
+#define DATTN_CLUSTER_PREFER_SMALL 0  // on a tie in CTAs: 0 fewer head groups, 1 smaller clusters
+#endif
+#ifndef DATTN_CLUSTER_FORCE_GROUPS
+#define DATTN_CLUSTER_FORCE_GROUPS 0  // > 0: only this many head groups (exploration)
+#endif
+#ifndef DATTN_CLUSTER_FORCE_SIZE
+#define DATTN_CLUSTER_FORCE_SIZE 0  // > 0: only clusters of this many CTAs (exploration)
+#endif
+constexpr int kClusterMaxBatch = DATTN_CLUSTER_MAX_BATCH;
 constexpr int kStageTargetBytes = DATTN_STAGE_BYTES_TWO_PER_SM;         // K+V per stage, 2 CTAs/SM
 constexpr int kStageTargetBytesOnePerSm = DATTN_STAGE_BYTES_ONE_PER_SM;  // K+V per stage, 1 CTA/SM
 constexpr int kTwoPerSmBudget = DATTN_RING_BYTES_TWO_PER_SM;  // ring bytes per CTA at 2 CTAs/SM
@@ -138,6 +170,8 @@ struct Plan {
     size_t prefix_bytes = 0, acc_bytes = 0, ws_bytes = 0;
     int combine_chunk = 0;  // channels per combine CTA
     int combine_inflight = 8;  // piece loads per combine thread per round
+    // cluster mode (see DecodeArgs::cluster): CTAs per cluster (0 = stream-K)
+    int cluster = 0, use_tmap = 0, inbox_offset = 0;
 };
 
 int next_pow2(int x) {
@@ -164,7 +198,7 @@ int validate_dims(int B, int H, int D, int S) {
     return DATTN_OK;
 }
 
-using PlanKey = std::tuple<int, int, int, int, int, int>;
+using PlanKey = std::tuple<int, int, int, int, int, int, bool>;
 std::mutex g_plan_mutex;
 std::map<PlanKey, Plan> g_plans;
 
@@ -187,7 +221,9 @@ int choose_partitions(const Plan &p, int B, int S) {
     return static_cast<int>(std::min<long long>({slots, by_work, kMaxPartitions}));
 }
 
-int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
+int make_cluster_plan(int B, int H, int D, int S, const DeviceInfo &di, Plan *out);
+
+int make_plan(int B, int H, int D, int S, int num_partitions, bool paged, Plan *out) {
     if (int st = validate_dims(B, H, D, S)) return st;
     if (num_partitions < 0)
         return fail(DATTN_ERR_INVALID_ARG, "num_partitions=%d must be >= 0", num_partitions);
@@ -195,7 +231,7 @@ int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
     if (int st = device_info(&di)) return st;
     int dev = 0;
     if (int st = current_device(&dev)) return st;
-    const PlanKey key{dev, B, H, D, S, num_partitions};
+    const PlanKey key{dev, B, H, D, S, num_partitions, paged};
     {
         std::lock_guard<std::mutex> lock(g_plan_mutex);
         auto it = g_plans.find(key);
@@ -299,11 +335,120 @@ int make_plan(int B, int H, int D, int S, int num_partitions, Plan *out) {
         const double per_thread = pieces / (128.0 / (cw / 4));
         p.combine_inflight = per_thread <= 2.0 ? 2 : (per_thread <= 4.0 ? 4 : 8);
     }
+    // Few sequences (dense cache, library-chosen partitions): one cluster of
+    // CTAs per (sequence, head group), merged in distributed shared memory,
+    // when such a plan exists.
+    if (num_partitions == 0 && !paged && B <= kClusterMaxBatch) {
+        Plan c;
+        if (int st = make_cluster_plan(B, H, D, S, di, &c)) return st;
+        if (c.cluster > 0) p = c;
+    }
     {
         std::lock_guard<std::mutex> lock(g_plan_mutex);
         g_plans[key] = p;
     }
     *out = p;
+    return DATTN_OK;
+}
+
+// Cluster plan: unit (b, g) of HG = H / NHG heads goes to one cluster of C
+// CTAs.  Among the head groupings whose K/V rows a tensor box can copy (or all
+// heads, one contiguous span per position) and the cluster sizes of which
+// B * NHG clusters fit on the GPU at once, take the one with the most CTAs
+// while each CTA still holds DATTN_CLUSTER_MIN_CTA_BYTES of K+V capacity; on a
+// tie, fewer head groups (longer rows).  out->cluster stays 0 when none fits.
+int make_cluster_plan(int B, int H, int D, int S, const DeviceInfo &di, Plan *out) {
+    *out = Plan();
+    const double cap_bytes = 4.0 * B * static_cast<double>(S) * H * D;  // K + V
+    if (cap_bytes > static_cast<double>(DATTN_CLUSTER_MAX_CAPACITY_BYTES)) return DATTN_OK;
+    if (static_cast<double>(B) * S >= 2147483647.0) return DATTN_OK;  // 32-bit box coordinate
+    const int c8 = D / 8;
+    int bdx, ch;
+    if (c8 <= 8) {
+        bdx = next_pow2(c8);
+        ch = 1;
+    } else if (c8 <= 16) {
+        bdx = 8;
+        ch = 2;
+    } else {
+        bdx = 16;
+        ch = 2;
+    }
+    const int kcap = ch == 2 ? 1 : 2;
+    Plan best;
+    long long best_ctas = 0;
+    for (int nhg = 1; nhg <= H; ++nhg) {
+        if (H % nhg != 0) continue;
+        if (DATTN_CLUSTER_FORCE_GROUPS > 0 && nhg != DATTN_CLUSTER_FORCE_GROUPS) continue;
+        const int hg = H / nhg;
+        if (hg * D * 4 > kMaxRowBytesKV) continue;
+        int nwc = DATTN_MIN_CONSUMER_WARPS > 8 ? 16 : 8;
+        if (hg > nwc * (32 / bdx) * kcap) nwc = 16;
+        const int nlg = nwc * (32 / bdx);
+        if (hg > nlg * kcap) continue;
+        Plan p;
+        p.sms = di.sms;
+        p.NHG = nhg;
+        p.HG = hg;
+        p.PHI = hg >= nlg ? 1 : std::min(32, nlg / hg);
+        const int kmax = (hg * p.PHI + nlg - 1) / nlg;
+        p.v = DecodeVariant{bdx, ch, kmax, nwc};
+        p.active_warps = std::min(nwc, (hg * p.PHI + (32 / bdx) - 1) / (32 / bdx));
+        const int row_bytes = hg * D * 2;
+        for (int C = DATTN_CLUSTER_MAX_SIZE; C >= 1; --C) {
+            if (DATTN_CLUSTER_FORCE_SIZE > 0 && C != DATTN_CLUSTER_FORCE_SIZE) continue;
+            const long long ctas = static_cast<long long>(B) * nhg * C;
+            if (ctas > static_cast<long long>(di.sms)) continue;
+            if (C > 1 && cap_bytes / static_cast<double>(ctas) < DATTN_CLUSTER_MIN_CTA_BYTES) continue;
+            // a stage: ~DATTN_CLUSTER_STAGE_BYTES of K+V, no more than a CTA's
+            // share of the capacity, a multiple of the phases
+            const int share = (S + C - 1) / C;
+            int P = std::max(1, std::min(256, DATTN_CLUSTER_STAGE_BYTES / 2 / row_bytes));
+            P = std::min(P, std::max(share, p.PHI));
+            P = std::max(p.PHI, P / p.PHI * p.PHI);
+            if (P > 256) continue;
+            // a head group's rows are copied as one tensor box {D, HG, P} per full stage
+            // (the box's shared-memory destination is 128-byte aligned)
+            const bool grouped = hg < H;
+            if (grouped && (static_cast<long long>(P) * row_bytes) % 128 != 0) continue;
+            const int merge_bytes = p.PHI > 1 ? hg * p.PHI * (D + 2) * 4 : 0;
+            // inbox: [C][HG] (m, l) pairs and [C][ceil(HG * D / C)] partial sums,
+            // then the CTA's own record [HG][D + 2]
+            const int inbox_bytes = (C * hg * 2 + C * ((hg * D + C - 1) / C) + hg * (D + 2)) * 4;
+            const int stage_bytes = 2 * P * row_bytes;
+            const int avail = di.max_smem_optin - kStaticSmemReserve - merge_bytes - inbox_bytes -
+                              16 * kMaxStages - 64;
+            const int nst = std::min(kMaxStages, avail / stage_bytes);
+            if (nst < 2) continue;
+            Plan q = p;
+            q.P = P;
+            q.NST = nst;
+            q.merge_offset = nst * stage_bytes;
+            q.inbox_offset = round_up(q.merge_offset + merge_bytes, 16);
+            q.bar_offset = round_up(q.inbox_offset + inbox_bytes, 16);
+            q.smem = q.bar_offset + nst * 16 + 16;
+            if (q.smem > di.max_smem_optin - kStaticSmemReserve) continue;
+            int clusters = 0;
+            cudaError_t e = dattn::decode_max_clusters(q.v, q.smem, C, &clusters);
+            if (e != cudaSuccess) {
+                cudaGetLastError();  // this cluster size is not available: try the next
+                continue;
+            }
+            if (clusters < B * nhg) continue;  // every cluster resident at once
+            const bool better =
+                ctas > best_ctas || (DATTN_CLUSTER_PREFER_SMALL && ctas == best_ctas && C < best.cluster);
+            if (!better) continue;
+            e = dattn::decode_occupancy(q.v, q.smem, &q.ctas_per_sm);
+            if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+            q.cluster = C;
+            q.use_tmap = grouped ? 1 : 0;
+            q.G = static_cast<int>(ctas);
+            q.ws_bytes = 0;
+            best = q;
+            best_ctas = ctas;
+        }
+    }
+    *out = best;
     return DATTN_OK;
 }
 
@@ -326,6 +471,41 @@ struct Paging {
     int page_size = 0, max_pages = 0;
 };
 
+// cuTensorMapEncodeTiled from the driver, found once through the runtime (the
+// driver library is not linked).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// Tensor map of a dense cache [B*S positions, H heads, D] (f16, innermost D)
+// whose box is one stage of one head group: {D, HG, P}.
+int encode_kv_box(CUtensorMap *map, const void *base, int B, int H, int D, int S, int HG, int P) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) return fail(DATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(B) * static_cast<cuuint64_t>(S)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                   static_cast<cuuint64_t>(H) * D * 2};  // bytes, dims 1 and 2
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(HG),
+                               static_cast<cuuint32_t>(P)};
+    const cuuint32_t unit[3] = {1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims,
+                           strides, box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+    return DATTN_OK;
+}
+
 int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, void *out, int B,
                   int H, int D, int S, const uint32_t *cur_pos, void *workspace,
                   cudaStream_t stream, const Paging &pg = Paging()) {
@@ -338,9 +518,10 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
     a.V = V;
     a.out = out;
     a.cur_pos = cur_pos;
-    a.ws_prefix = p.G > 1 ? reinterpret_cast<long long *>(ws) : nullptr;
-    a.ws_acc = p.G > 1 ? reinterpret_cast<float *>(ws + p.prefix_bytes) : nullptr;
-    a.ws_ml = p.G > 1 ? reinterpret_cast<float2 *>(ws + p.prefix_bytes + p.acc_bytes) : nullptr;
+    const bool split = p.G > 1 && p.cluster == 0;  // partial states go through the workspace
+    a.ws_prefix = split ? reinterpret_cast<long long *>(ws) : nullptr;
+    a.ws_acc = split ? reinterpret_cast<float *>(ws + p.prefix_bytes) : nullptr;
+    a.ws_ml = split ? reinterpret_cast<float2 *>(ws + p.prefix_bytes + p.acc_bytes) : nullptr;
     a.err = di.err_word;
     a.block_table = pg.table;
     a.num_pages = pg.num_pages;
@@ -363,9 +544,17 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
     // dense or paged cache: prefetch the first stages into L2 before the wait on
     // the previous kernel
     a.prefetch_positions = DATTN_PREFETCH_STAGES > 0 ? DATTN_PREFETCH_STAGES * p.P : 0;
+    a.cluster = p.cluster;
+    a.use_tmap = p.use_tmap;
+    a.inbox_offset = p.inbox_offset;
+    a.prefetch_threads = DATTN_PREFETCH_THREADS;
+    if (p.use_tmap) {
+        if (int st = encode_kv_box(&a.tmap_k, K, B, H, D, S, p.HG, p.P)) return st;
+        if (int st = encode_kv_box(&a.tmap_v, V, B, H, D, S, p.HG, p.P)) return st;
+    }
     cudaError_t e = dattn::launch_decode(a, p.v, p.smem, stream);
     if (e != cudaSuccess) return fail_cuda(e, "decode kernel launch");
-    if (p.G > 1) {
+    if (p.G > 1 && p.cluster == 0) {
         dattn::CombineArgs c{};
         c.ws_acc = a.ws_acc;
         c.ws_ml = a.ws_ml;
@@ -426,7 +615,7 @@ int dattn_decode_plan(int batch, int n_heads, int head_dim, int seq_len, int num
                       dattn_plan *plan) {
     if (plan == nullptr) return fail(DATTN_ERR_INVALID_ARG, "plan is NULL");
     Plan p;
-    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, &p)) return st;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, false, &p)) return st;
     plan->partitions = p.G;
     plan->heads_per_cta = p.HG;
     plan->head_groups = p.NHG;
@@ -437,15 +626,19 @@ int dattn_decode_plan(int batch, int n_heads, int head_dim, int seq_len, int num
     plan->ctas_per_sm = p.ctas_per_sm;
     plan->sm_count = p.sms;
     plan->workspace_bytes = p.ws_bytes;
+    plan->cluster_size = p.cluster;
     return DATTN_OK;
 }
 
 int dattn_decode_workspace_bytes(int batch, int n_heads, int head_dim, int seq_len,
                                  int num_partitions, size_t *bytes) {
     if (bytes == nullptr) return fail(DATTN_ERR_INVALID_ARG, "bytes is NULL");
-    Plan p;
-    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, &p)) return st;
-    *bytes = p.ws_bytes;
+    // enough for the dense call and for the paged call of the same capacity
+    // (a dense cache of few sequences may take the cluster plan, which needs none)
+    Plan p, q;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, false, &p)) return st;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, true, &q)) return st;
+    *bytes = std::max(p.ws_bytes, q.ws_bytes);
     return DATTN_OK;
 }
 
@@ -462,7 +655,7 @@ int dattn_decode_f16_ex(const void *Q, const void *K_cache, const void *V_cache,
     if (num_partitions < 0)
         return fail(DATTN_ERR_INVALID_ARG, "num_partitions=%d must be >= 0", num_partitions);
     Plan p;
-    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, &p)) return st;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, false, &p)) return st;
     if (p.ws_bytes > 0) {
         if (workspace == nullptr)
             return fail(DATTN_ERR_WORKSPACE, "workspace of %zu bytes required, got NULL",
@@ -486,7 +679,7 @@ int dattn_decode_f16(const void *Q, const void *K_cache, const void *V_cache, vo
     if (int st = check_tensor(out, "out")) return st;
     if (int st = check_cur_pos(current_pos)) return st;
     Plan p;
-    if (int st = make_plan(batch, n_heads, head_dim, seq_len, 0, &p)) return st;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, 0, false, &p)) return st;
     void *ws = nullptr;
     if (p.ws_bytes > 0) {
         int dev = 0;
@@ -545,7 +738,7 @@ int dattn_decode_paged_f16(const void *Q, const void *K_pages, const void *V_pag
     if (num_partitions < 0)
         return fail(DATTN_ERR_INVALID_ARG, "num_partitions=%d must be >= 0", num_partitions);
     Plan p;
-    if (int st = make_plan(batch, n_heads, head_dim, S, num_partitions, &p)) return st;
+    if (int st = make_plan(batch, n_heads, head_dim, S, num_partitions, true, &p)) return st;
     if (p.ws_bytes > 0) {
         if (workspace == nullptr)
             return fail(DATTN_ERR_WORKSPACE, "workspace of %zu bytes required, got NULL",

@@ -2,6 +2,7 @@
 // C-ABI layer (dattn_api.cpp) and the CUDA translation units.  Host-side types.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (a plain struct; the driver library is not linked)
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -34,6 +35,10 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // one second
 // f16 output of every unit it covers entirely and a partial softmax state for
 // the others.
 struct DecodeArgs {
+    // Cluster mode (cluster > 0) with a head group smaller than H: tiled tensor
+    // maps of K and V as [B*S positions, H, D] (innermost D), box {D, HG, P}.
+    // One box is one full stage of a head group.
+    CUtensorMap tmap_k, tmap_v;
     const void *Q;            // f16 [B,H,D]
     const void *K;            // f16 [B,S,H,D]
     const void *V;            // f16 [B,S,H,D]
@@ -64,6 +69,21 @@ struct DecodeArgs {
     // Positions of its first stages each CTA prefetches into L2 before waiting
     // on the kernel before it (0 = none).
     int prefetch_positions;
+    // Cluster mode: 0 = stream-K over the batch (above).  C > 0: the grid is
+    // head_groups * B clusters of C CTAs; cluster u takes unit u = (b, g) whole,
+    // CTA r of it the positions [r L_b / C, (r+1) L_b / C) of that unit, and
+    // the C partial states are merged through distributed shared memory into
+    // `out`.  No workspace and no second kernel.
+    int cluster;
+    int use_tmap;      // full stages of a head group are copied as one tensor box
+    // Cluster mode: byte offset of this CTA's inbox, where every CTA of the
+    // cluster stores its partial state for the outputs this CTA finishes:
+    // [C][HG] (m, l) pairs, then [C][ceil(HG*D / C)] partial sums; followed by
+    // the CTA's own record [HG][D + 2] (m, l, acc) that it pushes.
+    int inbox_offset;
+    // Pre-wait prefetch issued by every thread, one 128-byte line each (1), or
+    // by thread 0 as bulk prefetches on the TMA engine (0).
+    int prefetch_threads;
 };
 
 // Arguments of the combine kernel (log-sum-exp merge of the pieces of a unit).
@@ -93,6 +113,8 @@ struct DecodeVariant {
 cudaError_t launch_decode(const DecodeArgs &a, DecodeVariant v, int smem, cudaStream_t stream);
 // Resident CTAs per SM for a variant at a given dynamic shared memory size.
 cudaError_t decode_occupancy(DecodeVariant v, int smem, int *ctas_per_sm);
+// Clusters of `cluster` CTAs of a variant that can be resident at once.
+cudaError_t decode_max_clusters(DecodeVariant v, int smem, int cluster, int *clusters);
 // Raise the dynamic shared memory limit of every variant (once per device).
 cudaError_t decode_configure_smem(int max_smem);
 // Launch the combine kernel with programmatic dependent launch on `stream`.

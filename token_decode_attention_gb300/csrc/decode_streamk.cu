@@ -54,6 +54,7 @@ __device__ unsigned g_device_error = 0;
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int kMaxCluster = 16;  // CTAs per cluster in cluster mode (non-portable above 8)
 
 __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity) {
     return mbar_wait_bounded(bar, parity, kWaitLimitNs);
@@ -154,7 +155,7 @@ __device__ __forceinline__ bool next_piece(Walker &w, const DecodeArgs &a) {
 
 template <int BDX, int CH, int KMAX, int NWC>
 __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
-    decode_streamk_kernel(const DecodeArgs a) {
+    decode_streamk_kernel(const __grid_constant__ DecodeArgs a) {
     constexpr int NPOS = 2;              // positions per (head, phase) slot in a consumer group
     constexpr int BDY = 32 / BDX;        // lane groups per warp
     constexpr int NLG = NWC * BDY;       // lane groups per CTA
@@ -182,6 +183,11 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         fence_barrier_init();
     }
     __syncthreads();  // barrier initialisation visible to every warp
+    // Cluster mode: the shared memory of another CTA of the cluster may be
+    // written only once that CTA has started.  Every thread arrives here and
+    // waits after the CTA's range is known, by which time the other CTAs of
+    // the cluster (launched together) have long arrived.
+    if (a.cluster > 0) cluster_arrive_relaxed();
     // Launched with programmatic dependent launch: up to here only shared memory
     // is touched, so this CTA may already be resident while the kernel before it
     // on the stream finishes.  Everything after the wait sees that kernel's writes
@@ -199,13 +205,21 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     // kernel may still be writing: the entries read here are only used to pick
     // what to prefetch, each checked to lie inside the page pool, and are read
     // again after the wait for the copies.  A stale entry wastes a prefetch.
-    if (threadIdx.x == 0 && a.prefetch_positions > 0) {
+    if (a.prefetch_positions > 0 && (a.prefetch_threads || threadIdx.x == 0)) {
         const long long S = a.S, nhg = a.head_groups;
         // capacity (every sequence full): the host keeps c * Wc in 64 bits
         const long long Wc = static_cast<long long>(a.B) * nhg * S;
-        long long x = static_cast<long long>(blockIdx.x) * Wc / a.partitions;
-        const long long x_end =
-            min(x + a.prefetch_positions, static_cast<long long>(blockIdx.x + 1) * Wc / a.partitions);
+        long long x, x_lim;
+        if (a.cluster > 0) {  // CTA r of cluster u: [r S / C, (r+1) S / C) of unit u
+            const long long u = blockIdx.x / a.cluster;
+            const long long r = blockIdx.x - u * a.cluster;
+            x = u * S + r * S / a.cluster;
+            x_lim = u * S + (r + 1) * S / a.cluster;
+        } else {
+            x = static_cast<long long>(blockIdx.x) * Wc / a.partitions;
+            x_lim = static_cast<long long>(blockIdx.x + 1) * Wc / a.partitions;
+        }
+        const long long x_end = min(x + a.prefetch_positions, x_lim);
         const size_t row = static_cast<size_t>(a.H) * a.D;  // halves per position
         while (x < x_end) {
             const long long u = x / S;  // unit (b, g)
@@ -228,10 +242,37 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
             if (go) {
                 const __half *k0 = reinterpret_cast<const __half *>(a.K) + static_cast<size_t>(first_pos) * row;
                 const __half *v0 = reinterpret_cast<const __half *>(a.V) + static_cast<size_t>(first_pos) * row;
-                if (hg == a.H) {  // all heads: the run is one span
+                if (a.prefetch_threads) {
+                    // the SM's own L2 prefetches, one 128-byte line per thread at
+                    // a time, so the TMA engine stays free for the first copies
+                    const char *kb = reinterpret_cast<const char *>(k0);
+                    const char *vb = reinterpret_cast<const char *>(v0);
+                    if (hg == a.H) {  // the run is one span
+                        const long long bytes = n * static_cast<long long>(row) * 2;
+                        for (long long o = threadIdx.x * 128LL; o < bytes; o += blockDim.x * 128LL) {
+                            prefetch_l2_line(kb + o);
+                            prefetch_l2_line(vb + o);
+                        }
+                    } else {  // one span per position: a position per thread
+                        const int bytes = hg * a.D * 2;
+                        for (long long j = threadIdx.x; j < n; j += blockDim.x) {
+                            const size_t o = (static_cast<size_t>(j) * row + static_cast<size_t>(h0) * a.D) * 2;
+                            for (int c = 0; c < bytes; c += 128) {
+                                prefetch_l2_line(kb + o + c);
+                                prefetch_l2_line(vb + o + c);
+                            }
+                        }
+                    }
+                } else if (hg == a.H) {  // all heads: the run is one span
                     const uint32_t bytes = static_cast<uint32_t>(n * row * 2);
                     bulk_prefetch_l2(k0, bytes);
                     bulk_prefetch_l2(v0, bytes);
+                } else if (a.use_tmap) {  // a head group: whole tensor boxes of P positions
+                    for (long long j = 0; j + a.stage_pos <= n; j += a.stage_pos) {
+                        const int row0 = static_cast<int>(first_pos + j);
+                        tensor3d_prefetch_l2(&a.tmap_k, 0, h0, row0);
+                        tensor3d_prefetch_l2(&a.tmap_v, 0, h0, row0);
+                    }
                 } else {  // a head group: one span per position
                     const uint32_t bytes = static_cast<uint32_t>(hg) * a.D * 2;
                     for (long long j = 0; j < n; ++j) {
@@ -262,7 +303,19 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         x0 = range_begin_split(blockIdx.x, wq, wr, G);
         x1 = range_begin_split(blockIdx.x + 1, wq, wr, G);
     };
-    if (a.B <= 32) {
+    if (a.cluster > 0) {
+        // Cluster mode: CTA r of cluster u takes the positions
+        // [r L_b / C, (r+1) L_b / C) of unit u = (b, g), numbered from the
+        // start of sequence b; no scan over the batch.
+        const long long u = blockIdx.x / a.cluster;
+        const long long r = blockIdx.x - u * a.cluster;
+        b0 = u / nhg;
+        L0 = live_len(a.cur_pos, b0, a.S);
+        const long long g = u - b0 * nhg;
+        x0 = g * L0 + r * L0 / a.cluster;
+        x1 = g * L0 + (r + 1) * L0 / a.cluster;
+        base0 = 0;
+    } else if (a.B <= 32) {
         // Lane b holds sequence b: every warp scans the batch on its own, with
         // no shared memory and no CTA barrier.
         const long long Lb = lane < a.B ? live_len(a.cur_pos, lane, a.S) : 0;
@@ -337,9 +390,93 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     }
     // The combine kernel may begin launching; it waits for this grid to finish.
     pdl_launch_dependents();
-    if (x0 >= x1) return;  // empty range (fewer live positions than CTAs)
+    if (a.cluster > 0) cluster_wait();  // every CTA of the cluster has started
+
+    // Cluster mode.  The C CTAs of a cluster share the unit's E = HG x D
+    // outputs: CTA r finishes [r E / C, (r+1) E / C).  Each CTA first writes
+    // its partial state to a local record [HG][D + 2] (m, l, acc), then
+    // pushes it into the inbox of the CTAs that finish its outputs (remote
+    // shared-memory stores, no round trip): the (m, l) pair of every head to
+    // each CTA whose share touches the head, the partial sum of every output
+    // to its finisher.  After one cluster barrier every inbox is complete and
+    // each CTA merges its share from its own shared memory.  Share arithmetic
+    // is 32-bit (E <= 64 heads x 256 channels, C <= 16): output e belongs to
+    // CTA ((e + 1) C - 1) / E, whose share starts at r E / C.
+    const int crank = a.cluster > 0 ? static_cast<int>(blockIdx.x % a.cluster) : 0;
+    const int cl_E = a.heads_per_cta * D;
+    const int cl_share = a.cluster > 0 ? (cl_E + a.cluster - 1) / a.cluster : 0;
+    // inbox: [C][HG] (m, l), then [C][cl_share] partial sums; then the record
+    float *const inbox = reinterpret_cast<float *>(smem + a.inbox_offset);
+    float *const lrec = inbox + a.cluster * (2 * a.heads_per_cta + cl_share);
+    // push the local record: (m, l) of head h (i < HG) or partial sum i - HG
+    auto push_record = [&](int i) {
+        if (i < a.heads_per_cta) {
+            const int h = i;
+            const float m_ = lrec[h * (D + 2)], l_ = lrec[h * (D + 2) + 1];
+            const uint32_t local = smem_addr(inbox + 2 * (crank * a.heads_per_cta + h));
+            const int r1 = ((h + 1) * D * a.cluster - 1) / cl_E;
+            for (int r = ((h * D + 1) * a.cluster - 1) / cl_E; r <= r1; ++r) {
+                const uint32_t remote = cluster_map_shared(local, r);
+                st_shared_cluster_f32(remote, m_);
+                st_shared_cluster_f32(remote + 4u, l_);
+            }
+        } else {
+            const int e = i - a.heads_per_cta;
+            const int h = e / D;
+            const int r = ((e + 1) * a.cluster - 1) / cl_E;
+            const int e0 = r * cl_E / a.cluster;
+            const float v = lrec[h * (D + 2) + 2 + (e - h * D)];
+            const uint32_t local =
+                smem_addr(inbox + 2 * a.cluster * a.heads_per_cta + crank * cl_share + (e - e0));
+            st_shared_cluster_f32(cluster_map_shared(local, r), v);
+        }
+    };
+    // every thread of every CTA of the cluster calls this once, after its pushes
+    auto cluster_tail = [&]() {
+        cluster_sync_all();  // every push of the cluster has landed
+        const long long u = blockIdx.x / a.cluster;
+        const long long b = u / nhg;
+        const int h0 = static_cast<int>(u - b * nhg) * a.heads_per_cta;
+        const int e0 = crank * cl_E / a.cluster;
+        const int e1 = (crank + 1) * cl_E / a.cluster;
+        for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+            const int h = e / D;
+            float M = -INFINITY;
+            for (int j = 0; j < a.cluster; ++j) {
+                const float *ml = inbox + 2 * (j * a.heads_per_cta + h);
+                if (ml[1] > 0.f) M = fmaxf(M, ml[0]);
+            }
+            float L = 0.f, N = 0.f;
+            for (int j = 0; j < a.cluster; ++j) {
+                const float *ml = inbox + 2 * (j * a.heads_per_cta + h);
+                if (ml[1] > 0.f) {  // a CTA without positions sent an empty state
+                    const float w = fast_exp2(ml[0] - M);
+                    L = fmaf(w, ml[1], L);
+                    N = fmaf(w, inbox[2 * a.cluster * a.heads_per_cta + j * cl_share + (e - e0)], N);
+                }
+            }
+            reinterpret_cast<__half *>(a.out)[(static_cast<size_t>(b) * a.H + h0) * D + e] =
+                __float2half_rn(N / L);
+        }
+    };
+
+    if (x0 >= x1) {  // empty range (fewer live positions than CTAs)
+        if (a.cluster > 0) {  // an empty state for every head
+            for (int h = threadIdx.x; h < a.heads_per_cta; h += blockDim.x) {
+                lrec[h * (D + 2)] = -INFINITY;
+                lrec[h * (D + 2) + 1] = 0.f;
+            }
+            __syncthreads();
+            for (int h = threadIdx.x; h < a.heads_per_cta; h += blockDim.x) push_record(h);
+            cluster_tail();
+        }
+        return;
+    }
     // consumer warps whose lane groups hold no (head, phase) slot have nothing to do
-    if (warp < NWC && warp >= a.active_warps) return;
+    if (warp < NWC && warp >= a.active_warps) {
+        if (a.cluster > 0) cluster_tail();
+        return;
+    }
 
     Walker walk;
     walk.x = x0;
@@ -356,6 +493,9 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         const uint64_t policy = l2_evict_first_policy();
         const size_t pos_stride = static_cast<size_t>(a.H) * D;  // halves between positions
         const bool paged = a.block_table != nullptr;
+        // tensor boxes need a 128-byte aligned destination; otherwise the
+        // per-position copies below serve (same data, more copies)
+        const bool tmap_ok = a.use_tmap && (smem_addr(smem) & 127u) == 0;
         int st = 0, issued = 0;
         bool go = true;
         while (go && next_piece(walk, a)) {
@@ -399,6 +539,15 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                         if (lane == 0) {
                             bulk_g2s(dK, sK, np * row_bytes, &full_bar[slot], policy);
                             bulk_g2s(dV, sV, np * row_bytes, &full_bar[slot], policy);
+                        }
+                    } else if (tmap_ok && np == a.stage_pos) {
+                        // a full stage of the head group: one tensor box each
+                        // ({D, HG, P} at row b*S + pos0; the host checked that
+                        // B*S fits the 32-bit coordinate)
+                        if (lane == 0) {
+                            const int row0 = static_cast<int>(walk.b * a.S + pos0);
+                            tensor3d_g2s(dK, &a.tmap_k, 0, h0, row0, &full_bar[slot], policy);
+                            tensor3d_g2s(dV, &a.tmap_v, 0, h0, row0, &full_bar[slot], policy);
                         }
                     } else {
                         for (int j = lane; j < np; j += 32) {
@@ -458,6 +607,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                     atomicOr(a.err, kErrDrainWait);
             }
         }
+        if (a.cluster > 0) cluster_tail();
         return;
     }
 
@@ -491,7 +641,9 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     while (next_piece(walk, a)) {
         const int h0 = walk.g * a.heads_per_cta;
         const int hg = min(a.heads_per_cta, a.H - h0);
-        const bool final_piece = (walk.off == 0 && walk.len == walk.Lb);
+        // a unit this CTA covers whole gets its f16 output here (in cluster mode
+        // every output goes through the cluster merge)
+        const bool final_piece = a.cluster == 0 && walk.off == 0 && walk.len == walk.Lb;
         const int pstride = a.phases * hg * D;  // halves between a slot's consecutive positions
         const long long slot_id = piece_slot(blockIdx.x, walk.u);
         const __half *Qb =
@@ -638,6 +790,19 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                                 pack8_f16(&acc[k][i * 8], inv);
                         }
                     }
+                } else if (a.cluster > 0) {  // the local record of the head
+                    float *rec = lrec + hl[k] * (D + 2);
+                    if (lig == 0) {
+                        rec[0] = m[k];
+                        rec[1] = l[k];
+                    }
+#pragma unroll
+                    for (int i = 0; i < CH; ++i) {
+                        if (con[i]) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) rec[2 + (lig + BDX * i) * 8 + e] = acc[k][i * 8 + e];
+                        }
+                    }
                 } else {
                     const size_t row = static_cast<size_t>(slot_id) * a.heads_per_cta + hl[k];
 #pragma unroll
@@ -655,10 +820,44 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                 }
             }
         } else {
-            // several lane groups share a head: merge their states in shared memory
+            // Several lane groups share a head.  First, when the heads per CTA
+            // are a power of two below the lane groups per warp, the lane
+            // groups of one warp that hold the same head (lane offsets that are
+            // multiples of HG * BDX) merge their states with xor shuffles, and
+            // only the first HG lane groups of the warp keep a state: phases
+            // f = 0, fstep, 2 fstep, ...  Then the kept states are merged in
+            // shared memory.
+            const int hgc = a.heads_per_cta;
+            const bool wmerge = BDY > 1 && hgc < BDY && (hgc & (hgc - 1)) == 0;
+            const int fstep = wmerge ? BDY / hgc : 1;
+            if (wmerge) {
+#pragma unroll
+                for (int k = 0; k < KMAX; ++k) {
+                    if (!sv[k] || !write) {  // an empty state takes part in the exchange
+                        m[k] = -INFINITY;
+                        l[k] = 0.f;
+                    }
+                    for (int t = hgc; t < BDY; t <<= 1) {
+                        const int o = t * BDX;
+                        const float m2 = __shfl_xor_sync(kFull, m[k], o);
+                        const float l2 = __shfl_xor_sync(kFull, l[k], o);
+                        const float nm = fmaxf(m[k], m2);
+                        const float s1 = nm == -INFINITY ? 0.f : fast_exp2(m[k] - nm);
+                        const float s2 = nm == -INFINITY ? 0.f : fast_exp2(m2 - nm);
+                        l[k] = fmaf(l[k], s1, l2 * s2);
+#pragma unroll
+                        for (int i = 0; i < CH * 8; ++i) {
+                            const float a2 = __shfl_xor_sync(kFull, acc[k][i], o);
+                            acc[k][i] = fmaf(acc[k][i], s1, a2 * s2);
+                        }
+                        m[k] = nm;
+                    }
+                }
+            }
+            const bool keeper = !wmerge || (lane / BDX) < hgc;
 #pragma unroll
             for (int k = 0; k < KMAX; ++k) {
-                if (!sv[k] || !write) continue;
+                if (!sv[k] || !write || !keeper) continue;
                 float *r = mbuf + static_cast<size_t>(lg + k * NLG) * rec;
                 if (lig == 0) {
                     r[0] = m[k];
@@ -678,12 +877,12 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                 const int h = idx / D;
                 const int d = idx - h * D;
                 float M = -INFINITY;
-                for (int f = 0; f < a.phases; ++f) {
+                for (int f = 0; f < a.phases; f += fstep) {
                     const float *r = mbuf + static_cast<size_t>(f * a.heads_per_cta + h) * rec;
                     if (r[1] > 0.f) M = fmaxf(M, r[0]);
                 }
                 float lsum = 0.f, num = 0.f;
-                for (int f = 0; f < a.phases; ++f) {
+                for (int f = 0; f < a.phases; f += fstep) {
                     const float *r = mbuf + static_cast<size_t>(f * a.heads_per_cta + h) * rec;
                     if (r[1] > 0.f) {
                         const float w = fast_exp2(r[0] - M);
@@ -693,6 +892,13 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                 }
                 if (final_piece) {
                     reinterpret_cast<__half *>(a.out)[(bh0 + h) * D + d] = __float2half_rn(num / lsum);
+                } else if (a.cluster > 0) {  // the local record
+                    float *rec = lrec + h * (D + 2);
+                    rec[2 + d] = num;
+                    if (d == 0) {
+                        rec[0] = M;
+                        rec[1] = lsum;
+                    }
                 } else {
                     const size_t row = static_cast<size_t>(slot_id) * a.heads_per_cta + h;
                     a.ws_acc[row * D + d] = num;
@@ -701,6 +907,13 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
             }
             named_barrier_sync(1, consumer_threads);
         }
+    }
+    if (a.cluster > 0) {
+        // the record is complete (the phase merge ends with a barrier of the
+        // consumers; the single-phase epilogue needs one): push it
+        if (a.phases == 1) named_barrier_sync(1, consumer_threads);
+        for (int i = threadIdx.x; i < a.heads_per_cta + cl_E; i += consumer_threads) push_record(i);
+        cluster_tail();
     }
 }
 
@@ -758,11 +971,19 @@ cudaError_t launch_decode(const DecodeArgs &a, DecodeVariant v, int smem, cudaSt
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
     // the kernel waits (griddepcontrol.wait) before its first global-memory access
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (a.cluster > 0) {
+        if (a.cluster > kMaxCluster || a.partitions % a.cluster != 0) return cudaErrorInvalidValue;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(a.cluster);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
@@ -771,6 +992,23 @@ cudaError_t decode_occupancy(DecodeVariant v, int smem, int *ctas_per_sm) {
     if (fn == nullptr) return cudaErrorInvalidValue;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, decode_threads(v.nwc),
                                                          static_cast<size_t>(smem));
+}
+
+cudaError_t decode_max_clusters(DecodeVariant v, int smem, int cluster, int *clusters) {
+    const void *fn = variant_fn(v);
+    if (fn == nullptr || cluster < 1 || cluster > kMaxCluster) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cluster));
+    cfg.blockDim = dim3(decode_threads(v.nwc));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(clusters, fn, &cfg);
 }
 
 cudaError_t decode_configure_smem(int max_smem) {
@@ -786,6 +1024,9 @@ cudaError_t decode_configure_smem(int max_smem) {
         if (e != cudaSuccess) return e;
         const int dyn = max_smem - static_cast<int>(attr.sharedSizeBytes);
         e = cudaFuncSetAttribute(variant_fn(v), cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+        if (e != cudaSuccess) return e;
+        // cluster mode launches clusters of up to 16 CTAs
+        e = cudaFuncSetAttribute(variant_fn(v), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

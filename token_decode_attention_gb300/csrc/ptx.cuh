@@ -1,6 +1,7 @@
 // ptx.cuh -- inline-PTX helpers for sm_103a: mbarriers, bulk asynchronous
-// copies (TMA engine, non-tensor form), bounded waits and programmatic
-// dependent launch.
+// copies (TMA engine, plain and tiled-tensor forms), bounded waits,
+// thread-block cluster shared memory and barriers, and programmatic dependent
+// launch.
 #pragma once
 
 #include <cstdint>
@@ -109,11 +110,73 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Tiled bulk tensor copy global -> shared of one 3D box (TMA engine), described
+// by a tensor map in kernel parameter space (a __grid_constant__ argument);
+// coordinates innermost first.  Completion counted on `bar` in bytes.  dst is
+// 128-byte aligned.
+__device__ __forceinline__ void tensor3d_g2s(void *dst, const void *tmap, int c0, int c1, int c2,
+                                             uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar)),
+        "l"(policy)
+        : "memory");
+}
+
+// L2 prefetch of one 3D box of a tensor map (a hint, like bulk_prefetch_l2).
+__device__ __forceinline__ void tensor3d_prefetch_l2(const void *tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+// Thread-block clusters: rank of this CTA in its cluster, the address of the
+// same shared-memory location in another CTA of the cluster, a load from it,
+// and the cluster-wide barrier (every thread of every CTA of the cluster
+// arrives; release/acquire order shared-memory writes before it with reads
+// after it, across the cluster).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_map_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// The two halves of the barrier, for a split arrive ... wait.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait;" ::: "memory");
+}
+
 // Bulk prefetch of `bytes` (a multiple of 16) of global memory into L2.  A hint:
 // it moves no data into the CTA and cannot make a later read see stale values
 // (L2 is the point of coherence).
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Prefetch of the 128-byte line holding `p` into L2 (a hint, issued by the SM
+// itself rather than the TMA engine).
+__device__ __forceinline__ void prefetch_l2_line(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // Programmatic dependent launch: let the next kernel on the stream start
