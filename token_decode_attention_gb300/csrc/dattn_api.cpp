@@ -171,7 +171,7 @@ struct Plan {
     int combine_chunk = 0;  // channels per combine CTA
     int combine_inflight = 8;  // piece loads per combine thread per round
     // cluster mode (see DecodeArgs::cluster): CTAs per cluster (0 = stream-K)
-    int cluster = 0, use_tmap = 0, inbox_offset = 0;
+    int cluster = 0, use_tmap = 0, rec_offset = 0;
 };
 
 int next_pow2(int x) {
@@ -412,11 +412,9 @@ int make_cluster_plan(int B, int H, int D, int S, const DeviceInfo &di, Plan *ou
             const bool grouped = hg < H;
             if (grouped && (static_cast<long long>(P) * row_bytes) % 128 != 0) continue;
             const int merge_bytes = p.PHI > 1 ? hg * p.PHI * (D + 2) * 4 : 0;
-            // inbox: [C][HG] (m, l) pairs and [C][ceil(HG * D / C)] partial sums,
-            // then the CTA's own record [HG][D + 2]
-            const int inbox_bytes = (C * hg * 2 + C * ((hg * D + C - 1) / C) + hg * (D + 2)) * 4;
+            const int rec_bytes = hg * (D + 2) * 4;  // the CTA's record (m, l, acc) per head
             const int stage_bytes = 2 * P * row_bytes;
-            const int avail = di.max_smem_optin - kStaticSmemReserve - merge_bytes - inbox_bytes -
+            const int avail = di.max_smem_optin - kStaticSmemReserve - merge_bytes - rec_bytes -
                               16 * kMaxStages - 64;
             const int nst = std::min(kMaxStages, avail / stage_bytes);
             if (nst < 2) continue;
@@ -424,8 +422,8 @@ int make_cluster_plan(int B, int H, int D, int S, const DeviceInfo &di, Plan *ou
             q.P = P;
             q.NST = nst;
             q.merge_offset = nst * stage_bytes;
-            q.inbox_offset = round_up(q.merge_offset + merge_bytes, 16);
-            q.bar_offset = round_up(q.inbox_offset + inbox_bytes, 16);
+            q.rec_offset = round_up(q.merge_offset + merge_bytes, 16);
+            q.bar_offset = round_up(q.rec_offset + rec_bytes, 16);
             q.smem = q.bar_offset + nst * 16 + 16;
             if (q.smem > di.max_smem_optin - kStaticSmemReserve) continue;
             int clusters = 0;
@@ -546,7 +544,7 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
     a.prefetch_positions = DATTN_PREFETCH_STAGES > 0 ? DATTN_PREFETCH_STAGES * p.P : 0;
     a.cluster = p.cluster;
     a.use_tmap = p.use_tmap;
-    a.inbox_offset = p.inbox_offset;
+    a.rec_offset = p.rec_offset;
     a.prefetch_threads = DATTN_PREFETCH_THREADS;
     if (p.use_tmap) {
         if (int st = encode_kv_box(&a.tmap_k, K, B, H, D, S, p.HG, p.P)) return st;

@@ -76,11 +76,9 @@ struct DecodeArgs {
     // `out`.  No workspace and no second kernel.
     int cluster;
     int use_tmap;      // full stages of a head group are copied as one tensor box
-    // Cluster mode: byte offset of this CTA's inbox, where every CTA of the
-    // cluster stores its partial state for the outputs this CTA finishes:
-    // [C][HG] (m, l) pairs, then [C][ceil(HG*D / C)] partial sums; followed by
-    // the CTA's own record [HG][D + 2] (m, l, acc) that it pushes.
-    int inbox_offset;
+    // Cluster mode: byte offset of this CTA's record [HG][D + 2] of its
+    // partial state (m, l, acc) per head, read by the cluster's other CTAs.
+    int rec_offset;
     // Pre-wait prefetch issued by every thread, one 128-byte line each (1), or
     // by thread 0 as bulk prefetches on the TMA engine (0).
     int prefetch_threads;

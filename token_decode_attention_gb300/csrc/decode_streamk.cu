@@ -183,11 +183,6 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         fence_barrier_init();
     }
     __syncthreads();  // barrier initialisation visible to every warp
-    // Cluster mode: the shared memory of another CTA of the cluster may be
-    // written only once that CTA has started.  Every thread arrives here and
-    // waits after the CTA's range is known, by which time the other CTAs of
-    // the cluster (launched together) have long arrived.
-    if (a.cluster > 0) cluster_arrive_relaxed();
     // Launched with programmatic dependent launch: up to here only shared memory
     // is touched, so this CTA may already be resident while the kernel before it
     // on the stream finishes.  Everything after the wait sees that kernel's writes
@@ -390,84 +385,73 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     }
     // The combine kernel may begin launching; it waits for this grid to finish.
     pdl_launch_dependents();
-    if (a.cluster > 0) cluster_wait();  // every CTA of the cluster has started
 
-    // Cluster mode.  The C CTAs of a cluster share the unit's E = HG x D
-    // outputs: CTA r finishes [r E / C, (r+1) E / C).  Each CTA first writes
-    // its partial state to a local record [HG][D + 2] (m, l, acc), then
-    // pushes it into the inbox of the CTAs that finish its outputs (remote
-    // shared-memory stores, no round trip): the (m, l) pair of every head to
-    // each CTA whose share touches the head, the partial sum of every output
-    // to its finisher.  After one cluster barrier every inbox is complete and
-    // each CTA merges its share from its own shared memory.  Share arithmetic
-    // is 32-bit (E <= 64 heads x 256 channels, C <= 16): output e belongs to
-    // CTA ((e + 1) C - 1) / E, whose share starts at r E / C.
-    const int crank = a.cluster > 0 ? static_cast<int>(blockIdx.x % a.cluster) : 0;
-    const int cl_E = a.heads_per_cta * D;
-    const int cl_share = a.cluster > 0 ? (cl_E + a.cluster - 1) / a.cluster : 0;
-    // inbox: [C][HG] (m, l), then [C][cl_share] partial sums; then the record
-    float *const inbox = reinterpret_cast<float *>(smem + a.inbox_offset);
-    float *const lrec = inbox + a.cluster * (2 * a.heads_per_cta + cl_share);
-    // push the local record: (m, l) of head h (i < HG) or partial sum i - HG
-    auto push_record = [&](int i) {
-        if (i < a.heads_per_cta) {
-            const int h = i;
-            const float m_ = lrec[h * (D + 2)], l_ = lrec[h * (D + 2) + 1];
-            const uint32_t local = smem_addr(inbox + 2 * (crank * a.heads_per_cta + h));
-            const int r1 = ((h + 1) * D * a.cluster - 1) / cl_E;
-            for (int r = ((h * D + 1) * a.cluster - 1) / cl_E; r <= r1; ++r) {
-                const uint32_t remote = cluster_map_shared(local, r);
-                st_shared_cluster_f32(remote, m_);
-                st_shared_cluster_f32(remote + 4u, l_);
-            }
-        } else {
-            const int e = i - a.heads_per_cta;
-            const int h = e / D;
-            const int r = ((e + 1) * a.cluster - 1) / cl_E;
-            const int e0 = r * cl_E / a.cluster;
-            const float v = lrec[h * (D + 2) + 2 + (e - h * D)];
-            const uint32_t local =
-                smem_addr(inbox + 2 * a.cluster * a.heads_per_cta + crank * cl_share + (e - e0));
-            st_shared_cluster_f32(cluster_map_shared(local, r), v);
-        }
-    };
-    // every thread of every CTA of the cluster calls this once, after its pushes
+    // Cluster mode.  Each CTA writes its partial state (m, l, acc) per head to
+    // a record [HG][D + 2] in its own shared memory (a CTA without positions
+    // writes empty ones).  After a cluster barrier the C CTAs share the
+    // unit's E = HG x D outputs, CTA r finishing [r E / C, (r+1) E / C): it
+    // reads the C records of each output through distributed shared memory
+    // (all loads of an output issued together) and merges them.  A second,
+    // relaxed barrier keeps every record alive until all reads are done.
+    // (Pushing the records into the finishers' shared memory instead, with
+    // remote stores and a single barrier, measured slower.)
+    float *const lrec = reinterpret_cast<float *>(smem + a.rec_offset);
+    // every thread of every CTA of the cluster calls this once, after its record
     auto cluster_tail = [&]() {
-        cluster_sync_all();  // every push of the cluster has landed
-        const long long u = blockIdx.x / a.cluster;
+        cluster_sync_all();  // every record of the cluster is complete
+        const int C = a.cluster;
+        const long long u = blockIdx.x / C;
+        const int r = static_cast<int>(blockIdx.x - u * C);
         const long long b = u / nhg;
         const int h0 = static_cast<int>(u - b * nhg) * a.heads_per_cta;
-        const int e0 = crank * cl_E / a.cluster;
-        const int e1 = (crank + 1) * cl_E / a.cluster;
-        for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+        const int E = a.heads_per_cta * D;  // (32-bit: E <= 64 heads x 256 channels, C <= 16)
+        const int e1 = (r + 1) * E / C;
+        const uint32_t rec0 = smem_addr(lrec);
+        for (int e = r * E / C + threadIdx.x; e < e1; e += blockDim.x) {
             const int h = e / D;
-            float M = -INFINITY;
-            for (int j = 0; j < a.cluster; ++j) {
-                const float *ml = inbox + 2 * (j * a.heads_per_cta + h);
-                if (ml[1] > 0.f) M = fmaxf(M, ml[0]);
+            const int d = e - h * D;
+            const uint32_t hrec = rec0 + static_cast<uint32_t>(h * (D + 2)) * 4u;
+            float mj[kMaxCluster], lj[kMaxCluster], nj[kMaxCluster];
+#pragma unroll
+            for (int j = 0; j < kMaxCluster; ++j) {
+                mj[j] = -INFINITY;
+                lj[j] = 0.f;
+                nj[j] = 0.f;
+                if (j < C) {
+                    const uint32_t rr = cluster_map_shared(hrec, j);
+                    mj[j] = ld_shared_cluster_f32(rr);
+                    lj[j] = ld_shared_cluster_f32(rr + 4u);
+                    nj[j] = ld_shared_cluster_f32(rr + 8u + 4u * d);
+                }
             }
+            float M = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < kMaxCluster; ++j)
+                if (lj[j] > 0.f) M = fmaxf(M, mj[j]);
             float L = 0.f, N = 0.f;
-            for (int j = 0; j < a.cluster; ++j) {
-                const float *ml = inbox + 2 * (j * a.heads_per_cta + h);
-                if (ml[1] > 0.f) {  // a CTA without positions sent an empty state
-                    const float w = fast_exp2(ml[0] - M);
-                    L = fmaf(w, ml[1], L);
-                    N = fmaf(w, inbox[2 * a.cluster * a.heads_per_cta + j * cl_share + (e - e0)], N);
+#pragma unroll
+            for (int j = 0; j < kMaxCluster; ++j) {
+                if (lj[j] > 0.f) {  // an empty record holds no acc
+                    const float w = fast_exp2(mj[j] - M);
+                    L = fmaf(w, lj[j], L);
+                    N = fmaf(w, nj[j], N);
                 }
             }
             reinterpret_cast<__half *>(a.out)[(static_cast<size_t>(b) * a.H + h0) * D + e] =
                 __float2half_rn(N / L);
         }
+        // the loads above have returned (their values were used): a relaxed
+        // arrive is enough to keep every record alive until then
+        cluster_arrive_relaxed();
+        cluster_wait();
     };
 
     if (x0 >= x1) {  // empty range (fewer live positions than CTAs)
-        if (a.cluster > 0) {  // an empty state for every head
+        if (a.cluster > 0) {  // an empty record for every head
             for (int h = threadIdx.x; h < a.heads_per_cta; h += blockDim.x) {
                 lrec[h * (D + 2)] = -INFINITY;
                 lrec[h * (D + 2) + 1] = 0.f;
             }
-            __syncthreads();
-            for (int h = threadIdx.x; h < a.heads_per_cta; h += blockDim.x) push_record(h);
             cluster_tail();
         }
         return;
@@ -908,13 +892,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
             named_barrier_sync(1, consumer_threads);
         }
     }
-    if (a.cluster > 0) {
-        // the record is complete (the phase merge ends with a barrier of the
-        // consumers; the single-phase epilogue needs one): push it
-        if (a.phases == 1) named_barrier_sync(1, consumer_threads);
-        for (int i = threadIdx.x; i < a.heads_per_cta + cl_E; i += consumer_threads) push_record(i);
-        cluster_tail();
-    }
+    if (a.cluster > 0) cluster_tail();
 }
 
 // Instances: lanes per row x chunks per lane x slots per lane group x consumer
