@@ -412,11 +412,15 @@ class Replica:
                 "note": "each step its own graph launch (not overlapped with the previous one)"}
 
     def e2e(self, steps: int, warmup: int, stream):
-        """Same metric through the public API with host buffers.  Each step copies
+        """Same metric through the public API with host buffers.  Each step takes
         the new token's inputs (q, k, v rows and current_pos, packed in one pinned
-        host buffer) to the device in one copy, rotates q and k at current_pos and
-        appends k, v to the cache (dattn_rope_append_f16), runs the decode and
-        copies out back into pinned host memory.  The KV cache itself is
+        host buffer) from the host, rotates q and k at current_pos and appends k,
+        v to the cache (dattn_rope_append_f16), runs the decode and returns out
+        into pinned host memory.  The kernels read and write the pinned buffers
+        themselves over the CPU-GPU link (unified addressing): every step moves
+        the inputs host-to-device and the output device-to-host without a
+        copy-engine transfer.  The same step with cudaMemcpyAsync copies in and
+        out is measured beside it ('copy_engine').  The KV cache itself is
         device-resident state."""
         if self.page_size:
             return None  # measured on the dense layout only
@@ -434,18 +438,27 @@ class Replica:
         halves[n:2 * n].copy_(k_rows.reshape(-1))
         halves[2 * n:].copy_(v_rows.reshape(-1))
         pack_h[6 * n:].view(torch.int32).copy_(x["cur_pos"].cpu())
+        qh, kh, vh = (halves[i * n:(i + 1) * n].view(B, H, D) for i in range(3))
+        cph = pack_h[6 * n:].view(torch.int32)
+        out_h = torch.empty((B, H, D), dtype=torch.float16).pin_memory()
+        q_rot = torch.empty((B, H, D), dtype=torch.float16, device=self.device)
+        out_d = self.outs[0]
+        # the copy-engine variant's device-side buffers
         pack_d = torch.empty(pack_h.shape, dtype=torch.uint8, device=self.device)
         dh = pack_d[: 6 * n].view(torch.float16)
         q_d, knew_d, vnew_d = (dh[i * n:(i + 1) * n].view(B, H, D) for i in range(3))
         cp_d = pack_d[6 * n:].view(torch.int32)
-        out_h = torch.empty((B, H, D), dtype=torch.float16).pin_memory()
-        out_d = self.outs[0]
         h2d = pack_h.numel()
         d2h = out_h.numel() * 2
 
         stream.wait_stream(torch.cuda.current_stream(self.device))
 
         def one():
+            self.dattn.dattn_rope_append_f16(qh, kh, vh, q_rot, x["k"], x["v"], cph, stream=stream)
+            self.dattn.dattn_decode_f16_ex(q_rot, x["k"], x["v"], out_h, cph, self.ws,
+                                           self.partitions, stream)
+
+        def one_ce():
             pack_d.copy_(pack_h, non_blocking=True)
             self.dattn.dattn_rope_append_f16(q_d, knew_d, vnew_d, q_d, x["k"], x["v"], cp_d,
                                              stream=stream)
@@ -465,28 +478,33 @@ class Replica:
             return start.elapsed_time(end) / steps, (time.perf_counter() - t0) * 1e3 / steps
 
         def median_of(windows):
-            # three timing windows of `steps` steps each; the step time settles at
-            # one of two levels per window (see the note), so one window alone is
-            # noisy: report the median window and list all three
+            # three timing windows of `steps` steps each: report the median
+            # window and list all three
             runs = sorted(windows, key=lambda r: r[0])
             return runs[len(runs) // 2], [r[0] * 1e3 for r in windows]
 
-        with torch.cuda.stream(stream):
-            for _ in range(warmup):
-                one()
-            torch.cuda.synchronize()
-            (eager_ms, eager_wall), eager_windows = median_of([timed(one) for _ in range(3)])
-            # the same step recorded once with the library's batch API (outside the
+        def batched(fn):
+            # the step recorded once with the library's batch API (outside the
             # timed region) and submitted as one batch per step
             self.dattn.dattn_batch_begin(stream)
-            one()
+            fn()
             batch = self.dattn.dattn_batch_end(stream)
             for _ in range(warmup):
                 batch.launch(stream)
             torch.cuda.synchronize()
-            (ms, wall), windows = median_of([timed(lambda: batch.launch(stream)) for _ in range(3)])
+            res = median_of([timed(lambda: batch.launch(stream)) for _ in range(3)])
             nodes = batch.nodes
             batch.close()
+            return res, nodes
+
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                one()
+                one_ce()
+            torch.cuda.synchronize()
+            (eager_ms, eager_wall), eager_windows = median_of([timed(one) for _ in range(3)])
+            ((ms, wall), windows), nodes = batched(one)
+            ((ce_ms, _), ce_windows), ce_nodes = batched(one_ce)
         return {"value": self.bytes_per_step / (ms * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": ms, "wall_ms_per_step": wall,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -496,12 +514,20 @@ class Replica:
                 "eager": {"value": self.bytes_per_step / (eager_ms * 1e-3) / 1e9,
                           "ms_per_step": eager_ms, "wall_ms_per_step": eager_wall,
                           "windows_us_per_step": [round(w, 2) for w in eager_windows]},
-                "note": "one H2D copy of the new token's q, k, v rows and current_pos from "
-                        "pinned memory, q and k rotated and the K/V row appended at "
-                        "current_pos (dattn_rope_append_f16), decode, out copied D2H into "
-                        "pinned memory; 'eager' issues the same calls from Python each step; "
-                        "the KV cache is device-resident state; value counts the decode's "
-                        "bytes only; the median of three timing windows"}
+                "copy_engine": {"value": self.bytes_per_step / (ce_ms * 1e-3) / 1e9,
+                                "ms_per_step": ce_ms,
+                                "windows_us_per_step": [round(w, 2) for w in ce_windows],
+                                "submission": f"one batch per step ({ce_nodes} recorded "
+                                              "operations: H2D copy, rope/append, decode, "
+                                              "D2H copy)"},
+                "note": "the rope/append kernel reads the new token's q, k, v rows and "
+                        "current_pos from one pinned host buffer and the decode writes out "
+                        "into pinned host memory, over the CPU-GPU link (unified "
+                        "addressing; no copy-engine transfer); 'eager' issues the same "
+                        "calls from Python each step; 'copy_engine' moves the same bytes "
+                        "with cudaMemcpyAsync before and after the kernels; the KV cache is "
+                        "device-resident state; value counts the decode's bytes only; the "
+                        "median of three timing windows"}
 
 
 def graph_time_us(fn, steps: int, warmup: int, stream, graph: bool = True) -> float:

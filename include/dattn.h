@@ -16,10 +16,16 @@
  *   - f16 tensors are passed as untyped pointers to IEEE binary16 data, dense
  *     and row-major in the layouts given below, and must be 16-byte aligned
  *     (the page's allocator hands out 16-byte aligned blocks; section "Testing").
- *   - Every tensor and current_pos array is a DEVICE pointer on the current CUDA
- *     device.  The caller owns all buffers and the stream; the library keeps no
- *     pointer after a call returns (like the page-3 C API, which wraps caller
- *     buffers and never frees them).
+ *   - Every tensor and current_pos array is a pointer the current CUDA device
+ *     can access: device memory, or page-locked host memory (cudaHostAlloc,
+ *     cudaMallocHost, cudaHostRegister), which under unified addressing has the
+ *     same address on the device.  The kernels read and write host memory over
+ *     the CPU-GPU link (NVLink-C2C on GB300), so a decode step can take the new
+ *     token's inputs from the host and return its output there without a
+ *     copy-engine transfer; the KV cache belongs in device memory.  The caller
+ *     owns all buffers and the stream; the library keeps no pointer after a call
+ *     returns (like the page-3 C API, which wraps caller buffers and never frees
+ *     them).
  *   - Calls are asynchronous: they only enqueue kernels on `stream` (NULL = the
  *     legacy default stream) and return.  The page's launcher waits after every
  *     dispatch (section "Commit, wait, and reading results back"); here the

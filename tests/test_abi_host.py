@@ -111,7 +111,7 @@ def test_plan_queries_reject_bad_arguments_on_host(lib):
     assert lib.dattn_decode_plan(1, 2, 64, 16, 0, None) == _native.ERR_INVALID_ARG
 
 
-def test_python_binding_rejects_cpu_tensors():
+def test_python_binding_rejects_pageable_cpu_tensors():
     import torch
     q = torch.zeros(1, 2, 64, dtype=torch.float16)
     k = torch.zeros(1, 16, 2, 64, dtype=torch.float16)

@@ -112,12 +112,15 @@ def _stream_handle(stream) -> int:
 
 
 def _tensor(t: torch.Tensor, name: str, shape=None, dtype=torch.float16) -> int:
+    """Raw pointer of a CUDA tensor, or of a pinned (page-locked) CPU tensor: with
+    unified addressing pinned host memory has the same address on the device, and
+    the kernels read or write it over the CPU-GPU link."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or a pinned CPU tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous (call .contiguous() first)")
     if shape is not None and tuple(t.shape) != tuple(shape):
