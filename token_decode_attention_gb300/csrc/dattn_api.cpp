@@ -223,23 +223,9 @@ int choose_partitions(const Plan &p, int B, int S) {
 
 int make_cluster_plan(int B, int H, int D, int S, const DeviceInfo &di, Plan *out);
 
-int make_plan(int B, int H, int D, int S, int num_partitions, bool paged, Plan *out) {
-    if (int st = validate_dims(B, H, D, S)) return st;
-    if (num_partitions < 0)
-        return fail(DATTN_ERR_INVALID_ARG, "num_partitions=%d must be >= 0", num_partitions);
-    DeviceInfo di;
-    if (int st = device_info(&di)) return st;
-    int dev = 0;
-    if (int st = current_device(&dev)) return st;
-    const PlanKey key{dev, B, H, D, S, num_partitions, paged};
-    {
-        std::lock_guard<std::mutex> lock(g_plan_mutex);
-        auto it = g_plans.find(key);
-        if (it != g_plans.end()) {
-            *out = it->second;
-            return DATTN_OK;
-        }
-    }
+// The split (stream-K) plan with at least `min_groups` head groups.
+int split_plan(int B, int H, int D, int S, int num_partitions, int min_groups,
+               const DeviceInfo &di, Plan *out) {
     Plan p;
     p.sms = di.sms;
     // lanes per KV row and 8-element chunks per lane
@@ -263,7 +249,7 @@ int make_plan(int B, int H, int D, int S, int num_partitions, bool paged, Plan *
     if (H > nwc * (32 / bdx) * kcap) nwc = 16;
     const int nlg = nwc * (32 / bdx);  // lane groups per CTA
     const int hg_max = std::min(nlg * kcap, std::max(1, kMaxRowBytesKV / (D * 4)));
-    p.NHG = std::max((H + hg_max - 1) / hg_max, std::min(H, DATTN_MIN_HEAD_GROUPS));
+    p.NHG = std::max((H + hg_max - 1) / hg_max, std::min(H, min_groups));
     p.HG = (H + p.NHG - 1) / p.NHG;
     p.NHG = (H + p.HG - 1) / p.HG;  // no empty group
     p.PHI = p.HG >= nlg ? 1 : std::min(32, nlg / p.HG);
@@ -335,6 +321,30 @@ int make_plan(int B, int H, int D, int S, int num_partitions, bool paged, Plan *
         const double per_thread = pieces / (128.0 / (cw / 4));
         p.combine_inflight = per_thread <= 2.0 ? 2 : (per_thread <= 4.0 ? 4 : 8);
     }
+    *out = p;
+    return DATTN_OK;
+}
+
+
+int make_plan(int B, int H, int D, int S, int num_partitions, bool paged, Plan *out) {
+    if (int st = validate_dims(B, H, D, S)) return st;
+    if (num_partitions < 0)
+        return fail(DATTN_ERR_INVALID_ARG, "num_partitions=%d must be >= 0", num_partitions);
+    DeviceInfo di;
+    if (int st = device_info(&di)) return st;
+    int dev = 0;
+    if (int st = current_device(&dev)) return st;
+    const PlanKey key{dev, B, H, D, S, num_partitions, paged};
+    {
+        std::lock_guard<std::mutex> lock(g_plan_mutex);
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) {
+            *out = it->second;
+            return DATTN_OK;
+        }
+    }
+    Plan p;
+    if (int st = split_plan(B, H, D, S, num_partitions, DATTN_MIN_HEAD_GROUPS, di, &p)) return st;
     // Few sequences (dense cache, library-chosen partitions): one cluster of
     // CTAs per (sequence, head group), merged in distributed shared memory,
     // when such a plan exists.
