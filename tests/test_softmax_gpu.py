@@ -153,3 +153,39 @@ def test_softmax_very_long_rows_with_masked_halves_and_nan():
     assert torch.isnan(out[2]).all() and not torch.isnan(out[4]).any()
     assert abs(float(out[3, 12345]) - 1.0) <= 1e-6 and float(out[3].abs().sum()) - float(out[3, 12345]) == 0.0
     assert torch.allclose(out[[0, 1, 4]].double().sum(dim=1).cpu(), torch.ones(3, dtype=torch.float64), atol=1e-5)
+
+
+@pytest.mark.parametrize("rows,cols", [(37, 65540), (9, 100004), (300, 128256), (5, 262144),
+                                       (3, 400000), (2, 600000)])
+def test_softmax_rows_held_by_a_cluster(rows, cols):
+    # aligned rows above 256 KB: a cluster of CTAs per row holds the row in
+    # shared memory (slices double-buffered, partial states merged through
+    # distributed shared memory); 600000 columns need more shared memory than
+    # a cluster offers and take the L2 path.  Row counts are not multiples of
+    # the resident clusters.  Row 0 has a masked slice, row 1 is masked but for
+    # one entry, the last row has a NaN near its end.
+    g = torch.Generator(device="cuda").manual_seed(rows + cols)
+    x = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+    x.normal_(0.0, 3.0, generator=g)
+    x[0, cols // 3: cols // 3 + cols // 4] = float("-inf")
+    if rows > 2:
+        x[1, :] = float("-inf")
+        x[1, cols - 5] = -3.0
+    x[rows - 1, cols - 7] = float("nan")
+    out = dattn.softmax(x)
+    torch.cuda.synchronize()
+    check(x, out)
+    assert (out[0, cols // 3: cols // 3 + cols // 4] == 0).all()
+    assert torch.isnan(out[rows - 1]).all()
+    if rows > 2:
+        assert abs(float(out[1, cols - 5]) - 1.0) <= 1e-6
+        assert float(out[1].abs().sum()) == float(out[1, cols - 5])  # every other entry is 0
+
+
+def test_softmax_cluster_rows_all_masked_row_is_nan():
+    x = torch.full((4, 131072), float("-inf"), dtype=torch.float32, device="cuda")
+    x[1:].normal_()
+    out = dattn.softmax(x)
+    torch.cuda.synchronize()
+    assert torch.isnan(out[0]).all() and not torch.isnan(out[1:]).any()
+    check(x, out)

@@ -906,8 +906,10 @@ int dattn_softmax_f32(const float *x, float *out, long long rows, int cols,
         return fail(DATTN_ERR_INVALID_ARG, "matrix is too large");
     if (cols > 1024 && rows > 0x7fffffffLL)
         return fail(DATTN_ERR_UNSUPPORTED, "at most 2^31-1 rows of more than 1024 columns");
-    const cudaError_t e =
-        dattn::launch_softmax(x, out, rows, cols, reinterpret_cast<cudaStream_t>(stream));
+    DeviceInfo di;
+    if (int st = device_info(&di)) return st;
+    const cudaError_t e = dattn::launch_softmax(x, out, rows, cols, di.err_word,
+                                                reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DATTN_OK : fail_cuda(e, "softmax kernel launch");
 }
 

@@ -152,7 +152,7 @@ cudaError_t launch_rope_append(const RopeAppendArgs &a, cudaStream_t stream);
 
 // Row softmax over the last dimension of a f32 [rows, cols] matrix.
 cudaError_t launch_softmax(const float *x, float *out, long long rows, int cols,
-                           cudaStream_t stream);
+                           unsigned *err, cudaStream_t stream);
 
 // Page-faithful split calls.
 cudaError_t launch_qk(const void *Q, const void *K, void *scores, int B, int H, int D, int S,

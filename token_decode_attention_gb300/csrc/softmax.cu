@@ -11,15 +11,23 @@
 //   rows up to 16384: one CTA of 256 or 512 threads per row, the row kept in
 //     registers (up to 32 values per thread), block max and sum through
 //     shared memory: one read, one write;
-//   longer rows (cols % 4 == 0, 16-byte aligned): one or two persistent CTAs
-//     per SM walk the rows; the first pass loads a row with an evict-last L2
-//     policy and computes the running (max, sum) with exp2, the second
-//     re-reads it from L2 and writes the output with streaming stores;
+//   longer rows up to 256 KB (cols % 4 == 0, 16-byte aligned): one or two
+//     persistent CTAs per SM walk the rows; the first pass loads a row with an
+//     evict-last L2 policy and computes the running (max, sum) with exp2, the
+//     second re-reads it from L2 and writes the output with streaming stores;
+//   aligned rows above 256 KB: a thread-block cluster per row holds the row
+//     in its CTAs' shared memory (bulk copies), merges the slices' (max, sum)
+//     through distributed shared memory and writes the output: one read, one
+//     write (rows too long for any cluster take the L2 path);
 //   otherwise: one CTA per row, a pass computing the running (max, sum) per
 //     thread merged across the block, then a pass writing the output.
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "dattn_internal.h"
 #include "ptx.cuh"
@@ -265,6 +273,159 @@ __global__ void __launch_bounds__(NT, kL2Threads / NT) softmax_l2_rows(const flo
     }
 }
 
+// Rows too long for the persistent CTAs to keep in L2 between their two passes
+// (above 256 KB a row, 152 rows in flight overflow L2 and part of the second
+// pass comes from HBM again): a thread-block cluster of C CTAs per row, each
+// CTA holding its slice of the row in shared memory.  The slice is loaded by
+// bulk asynchronous copies (TMA engine) into one of `nbuf` buffers, so later
+// rows' slices can land while this one is finished (with one buffer, the
+// other CTA on the SM does that).  Pass one computes the
+// slice's (max, sum of exp2); the C states are merged through distributed
+// shared memory behind one cluster barrier per row; pass two reads the slice
+// from shared memory and writes the output with streaming stores.  One HBM
+// read and one write per element, whatever the number of rows in flight.
+// Clusters walk the rows persistently (cluster q takes rows q, q + nq, ...).
+template <int NT, int MINB>
+__global__ void __launch_bounds__(NT, MINB) softmax_cluster_rows(const float *__restrict__ x,
+                                                                 float *__restrict__ out,
+                                                                 long long rows, int cols,
+                                                                 int slice_cap, int nbuf,
+                                                                 unsigned *err) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float sm_m[NT / 32], sm_l[NT / 32];
+    __shared__ int sm_nan[NT / 32];
+    __shared__ float s_M, s_L;
+    __shared__ float2 s_xch[2];  // this CTA's (max, sum) of the rows of each parity
+    __shared__ alignas(8) uint64_t s_bar[4];
+    float4 *const buf = reinterpret_cast<float4 *>(smem);  // [nbuf][slice_cap], nbuf <= 4
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned C = cluster_nctarank();
+    const unsigned rank = cluster_ctarank();
+    const long long q = blockIdx.x / C, nq = gridDim.x / C;
+    const int n4 = cols / 4;
+    const int f0 = static_cast<int>(static_cast<long long>(rank) * n4 / C);
+    const int nf = static_cast<int>(static_cast<long long>(rank + 1) * n4 / C) - f0;  // <= slice_cap
+    if (tid == 0) {
+        for (int k = 0; k < nbuf; ++k) mbar_init(&s_bar[k], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const uint64_t once = l2_evict_first_policy();
+    // thread 0: copy this CTA's slice of `row` into buffer b (16-byte aligned:
+    // cols % 4 == 0 and x is 16-byte aligned)
+    auto issue = [&](long long row, int b) {
+        const char *src = reinterpret_cast<const char *>(x + row * cols) + static_cast<size_t>(f0) * 16;
+        char *dst = reinterpret_cast<char *>(buf + static_cast<size_t>(b) * slice_cap);
+        const uint32_t bytes = static_cast<uint32_t>(nf) * 16u;
+        mbar_arrive_expect_tx(&s_bar[b], bytes);
+        for (uint32_t o = 0; o < bytes; o += 32768u)
+            bulk_g2s(dst + o, src + o, bytes - o < 32768u ? bytes - o : 32768u, &s_bar[b], once);
+    };
+    bool ok = true;  // false once a wait ran out: no more copies are issued
+    // this CTA's rows in order: row q + it * nq goes to buffer it % nbuf, as
+    // that buffer's (it / nbuf)-th fill
+    int issued = 0, waited = 0;
+    for (int k = 0; k < nbuf && q + k * nq < rows; ++k) {
+        if (tid == 0) issue(q + k * nq, k);
+        ++issued;
+    }
+    int it = 0;
+    for (long long row = q; row < rows; row += nq, ++it) {
+        const int b = it % nbuf;
+        const int xs = it & 1;  // exchange slot: rows alternate
+        const float4 *s4 = buf + static_cast<size_t>(b) * slice_cap;
+        if (ok) {
+            const bool done = mbar_wait_bounded(&s_bar[b], (it / nbuf) & 1, kWaitLimitNs);
+            if (!__syncthreads_and(done)) {
+                if (tid == 0) atomicOr(err, kErrConsumerWait);
+                ok = false;
+            } else {
+                ++waited;
+            }
+        }
+        // pass one: this slice's running (max, sum of 2^(x log2 e - S(max)))
+        float m = -INFINITY, l = 0.f;
+        bool nan = false;
+        for (int i = tid; i < nf; i += NT) {
+            const float4 t = s4[i];
+            nan |= isnan(t.x) || isnan(t.y) || isnan(t.z) || isnan(t.w);
+            const float M = fmaxf(m, fmaxf(fmaxf(t.x, t.y), fmaxf(t.z, t.w)));
+            if (M != -INFINITY) {
+                const float sM = __fmul_rn(M, kLog2e);
+                if (M > m) {
+                    l *= ex2(__fmul_rn(m, kLog2e) - sM);  // 0 while m is -inf
+                    m = M;
+                }
+                l += ex2(fmaf(t.x, kLog2e, -sM)) + ex2(fmaf(t.y, kLog2e, -sM)) +
+                     ex2(fmaf(t.z, kLog2e, -sM)) + ex2(fmaf(t.w, kLog2e, -sM));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+            const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+            merge2(m, l, m2, l2);
+        }
+        const bool warp_nan = __any_sync(0xffffffffu, nan);
+        if (lane == 0) {
+            sm_m[warp] = m;
+            sm_l[warp] = l;
+            sm_nan[warp] = warp_nan;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float M = sm_m[0], L = sm_l[0];
+            bool any_nan = sm_nan[0] != 0;
+            for (int w = 1; w < NT / 32; ++w) {
+                merge2(M, L, sm_m[w], sm_l[w]);
+                any_nan |= sm_nan[w] != 0;
+            }
+            s_xch[xs] = make_float2(M, any_nan ? NAN : L);  // a NaN sum marks a NaN
+        }
+        // every CTA's state of this row is visible to the cluster after this
+        cluster_sync_all();
+        if (warp == 0) {
+            float2 v = make_float2(-INFINITY, 0.f);
+            if (lane < static_cast<int>(C)) v = ld_shared_cluster_f2(cluster_map_shared(smem_addr(&s_xch[xs]), lane));
+            const bool row_nan = __any_sync(0xffffffffu, isnan(v.y));
+            float M = v.x, L = isnan(v.y) ? 0.f : v.y;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+                const float l2 = __shfl_xor_sync(0xffffffffu, L, o);
+                merge2(M, L, m2, l2);
+            }
+            if (lane == 0) {
+                s_M = M;
+                s_L = row_nan ? NAN : L;  // a NaN anywhere, or only -inf (0 / 0), gives a NaN row
+            }
+        }
+        __syncthreads();
+        const float inv = 1.f / s_L;
+        const float sm = __fmul_rn(s_M, kLog2e);
+        float4 *o4 = reinterpret_cast<float4 *>(out + row * cols) + f0;
+        for (int i = tid; i < nf; i += NT) {
+            const float4 t = s4[i];
+            __stcs(o4 + i, make_float4(ex2(fmaf(t.x, kLog2e, -sm)) * inv,
+                                       ex2(fmaf(t.y, kLog2e, -sm)) * inv,
+                                       ex2(fmaf(t.z, kLog2e, -sm)) * inv,
+                                       ex2(fmaf(t.w, kLog2e, -sm)) * inv));
+        }
+        __syncthreads();  // every thread is done with buffer b
+        if (ok && row + static_cast<long long>(nbuf) * nq < rows) {
+            if (tid == 0) issue(row + static_cast<long long>(nbuf) * nq, b);
+            ++issued;
+        }
+    }
+    // no copy may still be landing when the CTA exits (only after a wait ran out)
+    if (tid == 0) {
+        for (int k = waited; k < issued; ++k)
+            if (!mbar_wait_bounded(&s_bar[k % nbuf], (k / nbuf) & 1, kWaitLimitNs)) atomicOr(err, kErrDrainWait);
+    }
+    // no CTA leaves while another may still read its (max, sum)
+    cluster_sync_all();
+}
+
 __global__ void __launch_bounds__(kRowThreads) softmax_block_rows(const float *__restrict__ x,
                                                                   float *__restrict__ out,
                                                                   int cols, bool vec4) {
@@ -340,8 +501,93 @@ __global__ void __launch_bounds__(kRowThreads) softmax_block_rows(const float *_
 
 }  // namespace
 
+#ifndef DATTN_SOFTMAX_CLUSTER_MIN_COLS
+#define DATTN_SOFTMAX_CLUSTER_MIN_COLS (64 * 1024 + 1)  // rows above 256 KB
+#endif
+// Measured at 128256 and 262144 columns: one slice buffer per CTA and two
+// CTAs per SM (the other CTA's row hides each load) beat two or more buffers
+// with one, three or four CTAs per SM.
+#ifndef DATTN_SOFTMAX_CLUSTER_BUFFERS
+#define DATTN_SOFTMAX_CLUSTER_BUFFERS 1  // slices in flight per CTA (1 to 4)
+#endif
+#ifndef DATTN_SOFTMAX_CLUSTER_CTAS_PER_SM
+#define DATTN_SOFTMAX_CLUSTER_CTAS_PER_SM 2  // 1: 512 threads per CTA; more: 256
+#endif
+constexpr int kClusterRowThreads = DATTN_SOFTMAX_CLUSTER_CTAS_PER_SM == 1 ? 512 : 256;
+constexpr int kClusterRowMinBlocks = DATTN_SOFTMAX_CLUSTER_CTAS_PER_SM;
+constexpr int kClusterRowBuffers = DATTN_SOFTMAX_CLUSTER_BUFFERS;
+static_assert(kClusterRowBuffers >= 1 && kClusterRowBuffers <= 4, "1 to 4 slice buffers");
+
+// Launch configuration of softmax_cluster_rows for a row length: the smallest
+// cluster whose slices, double-buffered, fit the shared memory of one CTA, and
+// as many clusters as are resident at once (cached per device and length).
+struct ClusterRowsConfig {
+    int cluster = 0, slice_cap = 0, clusters = 0;
+    size_t smem = 0;
+};
+
+cudaError_t cluster_rows_config(int cols, ClusterRowsConfig *cfg_out) {
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, ClusterRowsConfig> cache;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find({dev, cols});
+    if (it != cache.end()) {
+        *cfg_out = it->second;
+        return cudaSuccess;
+    }
+    int max_smem = 0;
+    e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    const void *fn = reinterpret_cast<const void *>(softmax_cluster_rows<kClusterRowThreads, kClusterRowMinBlocks>);
+    cudaFuncAttributes attr{};
+    e = cudaFuncGetAttributes(&attr, fn);
+    if (e != cudaSuccess) return e;
+    const int dyn_max = max_smem - static_cast<int>(attr.sharedSizeBytes);
+    // shared memory per CTA when kClusterRowMinBlocks CTAs share an SM
+    const int per_sm = (max_smem + 1024) / kClusterRowMinBlocks - 1024 -
+                       static_cast<int>(attr.sharedSizeBytes);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    ClusterRowsConfig best;
+    const int n4 = cols / 4;
+    for (int c = 2; c <= 16; ++c) {
+        const int cap = (n4 + c - 1) / c;
+        const size_t smem = static_cast<size_t>(cap) * 16 * kClusterRowBuffers;
+        if (smem > static_cast<size_t>(std::min(dyn_max, per_sm))) continue;
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3(static_cast<unsigned>(c));
+        lc.blockDim = dim3(kClusterRowThreads);
+        lc.dynamicSmemBytes = smem;
+        cudaLaunchAttribute la[1];
+        la[0].id = cudaLaunchAttributeClusterDimension;
+        la[0].val.clusterDim.x = static_cast<unsigned>(c);
+        la[0].val.clusterDim.y = 1;
+        la[0].val.clusterDim.z = 1;
+        lc.attrs = la;
+        lc.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, fn, &lc) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (n < 1) continue;
+        best.cluster = c;
+        best.slice_cap = cap;
+        best.clusters = n;
+        best.smem = smem;
+        break;  // the smallest cluster that fits
+    }
+    cache[{dev, cols}] = best;
+    *cfg_out = best;
+    return cudaSuccess;
+}
+
 cudaError_t launch_softmax(const float *x, float *out, long long rows, int cols,
-                           cudaStream_t stream) {
+                           unsigned *err, cudaStream_t stream) {
     if (rows <= 0 || cols <= 0) return cudaErrorInvalidValue;
     if (cols <= kWarpRowMax) {
         const long long blocks = (rows + 7) / 8;
@@ -381,6 +627,29 @@ cudaError_t launch_softmax(const float *x, float *out, long long rows, int cols,
         void *args[] = {&x, &out, &cols};
         return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(rows)), dim3(kRowThreads), args, 0,
                                 stream);
+    }
+    if (vec4 && cols >= DATTN_SOFTMAX_CLUSTER_MIN_COLS) {
+        // rows above 256 KB: a cluster per row, the row held in shared memory
+        ClusterRowsConfig cc;
+        cudaError_t e = cluster_rows_config(cols, &cc);
+        if (e != cudaSuccess) return e;
+        if (cc.cluster > 0) {
+            const long long clusters = rows < cc.clusters ? rows : cc.clusters;
+            cudaLaunchConfig_t lc = {};
+            lc.gridDim = dim3(static_cast<unsigned>(clusters * cc.cluster));
+            lc.blockDim = dim3(kClusterRowThreads);
+            lc.dynamicSmemBytes = cc.smem;
+            lc.stream = stream;
+            cudaLaunchAttribute la[1];
+            la[0].id = cudaLaunchAttributeClusterDimension;
+            la[0].val.clusterDim.x = static_cast<unsigned>(cc.cluster);
+            la[0].val.clusterDim.y = 1;
+            la[0].val.clusterDim.z = 1;
+            lc.attrs = la;
+            lc.numAttrs = 1;
+            return cudaLaunchKernelEx(&lc, softmax_cluster_rows<kClusterRowThreads, kClusterRowMinBlocks>,
+                                      x, out, rows, cols, cc.slice_cap, kClusterRowBuffers, err);
+        }
     }
     if (vec4) {
         // long aligned rows: one or two persistent CTAs per SM walk the rows
