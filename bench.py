@@ -98,8 +98,8 @@ def hbm_peak() -> tuple[float, str]:
 
 
 # the sources of the decode call whose DRAM traffic profiles/ncu_traffic.json records
-DECODE_SOURCES = ("decode_streamk.cu", "combine.cu", "merge.cuh", "streamk.h", "ptx.cuh",
-                  "dattn_internal.h", "dattn_api.cpp")
+DECODE_SOURCES = ("decode_kernel.cuh", "decode_streamk.cu", "decode_cluster.cu", "combine.cu",
+                  "merge.cuh", "streamk.h", "ptx.cuh", "dattn_internal.h", "dattn_api.cpp")
 
 
 def _code_only(text: str) -> str:

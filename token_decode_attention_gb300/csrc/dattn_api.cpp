@@ -56,9 +56,6 @@ constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
 #ifndef DATTN_PREFETCH_STAGES
 #define DATTN_PREFETCH_STAGES 2  // stages each CTA prefetches into L2 before its wait (0: none)
 #endif
-#ifndef DATTN_PREFETCH_THREADS
-#define DATTN_PREFETCH_THREADS 0  // 1: every thread prefetches lines; 0: bulk prefetches (TMA)
-#endif
 #ifndef DATTN_MIN_HEAD_GROUPS
 #define DATTN_MIN_HEAD_GROUPS 1  // split the heads into at least this many groups
 #endif
@@ -555,7 +552,6 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
     a.cluster = p.cluster;
     a.use_tmap = p.use_tmap;
     a.rec_offset = p.rec_offset;
-    a.prefetch_threads = DATTN_PREFETCH_THREADS;
     if (p.use_tmap) {
         if (int st = encode_kv_box(&a.tmap_k, K, B, H, D, S, p.HG, p.P)) return st;
         if (int st = encode_kv_box(&a.tmap_v, V, B, H, D, S, p.HG, p.P)) return st;

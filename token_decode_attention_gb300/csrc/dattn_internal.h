@@ -79,9 +79,6 @@ struct DecodeArgs {
     // Cluster mode: byte offset of this CTA's record [HG][D + 2] of its
     // partial state (m, l, acc) per head, read by the cluster's other CTAs.
     int rec_offset;
-    // Pre-wait prefetch issued by every thread, one 128-byte line each (1), or
-    // by thread 0 as bulk prefetches on the TMA engine (0).
-    int prefetch_threads;
 };
 
 // Arguments of the combine kernel (log-sum-exp merge of the pieces of a unit).

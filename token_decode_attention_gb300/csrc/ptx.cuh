@@ -180,12 +180,6 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
-// Prefetch of the 128-byte line holding `p` into L2 (a hint, issued by the SM
-// itself rather than the TMA engine).
-__device__ __forceinline__ void prefetch_l2_line(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 // Programmatic dependent launch: let the next kernel on the stream start
 // launching, and (in that kernel) wait until the previous grid has completed
 // and its memory is visible.
