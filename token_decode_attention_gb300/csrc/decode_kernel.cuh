@@ -1,8 +1,10 @@
 // decode_kernel.cuh -- the fused decode-attention kernel template for sm_103a,
-// instantiated for the split plan in decode_streamk.cu and for the cluster plan
-// in decode_cluster.cu (two translation units, built in parallel; each
-// instance holds only its own plan's code, which keeps the latency-bound
-// launches of either plan lean).
+// instantiated for the split plan (dense and paged caches) in decode_streamk.cu
+// and for the cluster plan (dense caches) in decode_cluster.cu: two
+// translation units, built in parallel, each instance holding only its own
+// plan's code, which keeps the latency-bound launches of either plan lean.
+// (Separate dense and paged instances of the split plan were measured too:
+// the dense one ran long 1.3 % slower, so the split plan keeps one.)
 //
 // Computes, per sequence b and head h, the masked softmax attention of the
 // kernels attention_qk_f16 and attention_pv_f16 of "Developing Apple Metal
@@ -229,7 +231,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
             long long n = min(S - off, x_end - x);
             long long first_pos = b * S + off;  // dense: row index in [B*S]
             bool go = true;
-            if (a.block_table != nullptr) {
+            if (!CLUSTER && a.block_table != nullptr) {  // the cluster plan is dense only
                 const long long pidx = off / a.page_size;
                 const long long in_page = off - pidx * a.page_size;
                 n = min(n, static_cast<long long>(a.page_size) - in_page);
@@ -459,7 +461,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         // ---------------- producer warp ----------------
         const uint64_t policy = l2_evict_first_policy();
         const size_t pos_stride = static_cast<size_t>(a.H) * D;  // halves between positions
-        const bool paged = a.block_table != nullptr;
+        const bool paged = !CLUSTER && a.block_table != nullptr;  // the cluster plan is dense only
         // tensor boxes need a 128-byte aligned destination; otherwise the
         // per-position copies below serve (same data, more copies)
         const bool tmap_ok = CLUSTER && a.use_tmap && (smem_addr(smem) & 127u) == 0;
