@@ -140,10 +140,12 @@ struct Walker {
     long long u;
 };
 
+template <bool CLUSTER>
 __device__ __forceinline__ bool next_piece(Walker &w, const DecodeArgs &a) {
     if (w.x >= w.x1) return false;
     const long long nhg = a.head_groups;
-    while (w.x >= w.base + nhg * w.Lb) {
+    // a cluster-plan range lies inside one unit: no later sequence to move to
+    while (!CLUSTER && w.x >= w.base + nhg * w.Lb) {
         w.base += nhg * w.Lb;
         ++w.b;
         w.Lb = live_len(a.cur_pos, w.b, a.S);
@@ -467,7 +469,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         const bool tmap_ok = CLUSTER && a.use_tmap && (smem_addr(smem) & 127u) == 0;
         int st = 0, issued = 0;
         bool go = true;
-        while (go && next_piece(walk, a)) {
+        while (go && next_piece<CLUSTER>(walk, a)) {
             const int h0 = walk.g * a.heads_per_cta;
             const int hg = min(a.heads_per_cta, a.H - h0);
             const size_t seq_base = (static_cast<size_t>(walk.b) * a.S * a.H + h0) * D;
@@ -607,7 +609,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     // waiting on it.
     bool ok = true;
 
-    while (next_piece(walk, a)) {
+    while (next_piece<CLUSTER>(walk, a)) {
         const int h0 = walk.g * a.heads_per_cta;
         const int hg = min(a.heads_per_cta, a.H - h0);
         // a unit this CTA covers whole gets its f16 output here (in cluster mode
