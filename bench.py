@@ -690,7 +690,12 @@ def sweep(device, stream, l2_bytes: int, steps: int, warmup: int, peak: float) -
                          "frac_of_nominal_8TBs": gbs / NOMINAL_HBM_GBS,
                          "query_heads_per_s": r.w.batch * r.w.n_heads / t,
                          "isolated_step_us_p10_p50_p90": [pct["p10"], pct["p50"], pct["p90"]],
-                         "partitions": r.plan["partitions"],
+                         # a paged cache always takes the split plan, whose partition
+                         # count the dense plan query does not report when the dense
+                         # shape takes the cluster plan
+                         "plan": ("cluster" if r.plan["cluster_size"] and not ps else "split"),
+                         "partitions": (r.plan["partitions"]
+                                        if not (ps and r.plan["cluster_size"]) else None),
                          "algorithmic_bytes": r.bytes_per_step, "l2": r.l2_note}
             del r
         except Exception as e:  # report, keep going

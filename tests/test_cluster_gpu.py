@@ -156,3 +156,33 @@ def test_recorded_batch_replays_on_new_contents():
         ref = oracle.decode_f64(to_np(q), to_np(k), to_np(v), np.asarray([cp], np.uint32))
         assert_decode_close(out, ref, f"replay cp={cp}")
     batch.close()
+
+
+def draw_single_sequence_cases(n=120, seed=20261202):
+    """Seeded single-sequence shapes for the cluster plan: every head_dim class,
+    head counts with few and many divisors, live lengths from 1 to past seq_len."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        D = int(rng.integers(1, 33)) * 8
+        H = int(rng.choice([1, 2, 3, 4, 6, 7, 8, 12, 16, 24, 32, 40, 48, 64]))
+        S = int(rng.integers(1, 5000))
+        if S * H * D > 1.6e7:
+            continue
+        cp = int(rng.integers(0, S + 5)) if rng.random() < 0.8 else int(rng.integers(0, 40))
+        cases.append((H, D, S, cp, len(cases)))
+    return cases
+
+
+RANDOM_CASES = draw_single_sequence_cases()
+
+
+@pytest.mark.parametrize("H,D,S,cp,i", RANDOM_CASES,
+                         ids=[f"{c[4]}-H{c[0]}D{c[1]}S{c[2]}cp{c[3]}" for c in RANDOM_CASES])
+def test_random_single_sequence(H, D, S, cp, i):
+    g = torch.Generator(device="cuda").manual_seed(5000 + i)
+    q, k, v = rand_f16(g, (1, H, D)), rand_f16(g, (1, S, H, D)), rand_f16(g, (1, S, H, D))
+    out = dattn.decode(q, k, v, cur_pos_tensor([cp]))
+    torch.cuda.synchronize()
+    ref = oracle.decode_f64(to_np(q), to_np(k), to_np(v), np.asarray([cp], np.uint32))
+    assert_decode_close(out, ref, f"case {i}: plan {dattn.dattn_decode_plan(1, H, D, S)}")
