@@ -23,6 +23,14 @@
 // for combine.cu.  Positions past L_b belong to no range: the page's -infinity
 // mask is a loop bound and masked rows are never read.
 //
+// Cluster plan (the CLUSTER instances; a dense cache of one sequence): the grid
+// is B * NHG thread-block clusters of C CTAs.  Cluster u takes unit u whole and
+// CTA r of it the positions [r L_b / C, (r+1) L_b / C); a head group smaller
+// than H is copied per full stage as one 3D tensor box {D, HG, P}.  Each CTA
+// leaves its partial state in a shared-memory record, and the cluster's CTAs
+// merge the C records through distributed shared memory, each finishing an
+// equal share of the unit's outputs: no workspace and no second kernel.
+//
 // Per CTA:
 //   * launched with programmatic dependent launch, it initialises its barriers
 //     and prefetches the first stages of its likely range into L2 before
@@ -391,7 +399,9 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         const int r = static_cast<int>(blockIdx.x - u * C);
         const long long b = u / nhg;
         const int h0 = static_cast<int>(u - b * nhg) * a.heads_per_cta;
-        const int E = a.heads_per_cta * D;  // (32-bit: E <= 64 heads x 256 channels, C <= 16)
+        // 32-bit share arithmetic: E = HG * D <= 12288 (the plan keeps a position's
+        // K+V rows of a group within 48 KB) and C <= 16
+        const int E = a.heads_per_cta * D;
         const int e1 = (r + 1) * E / C;
         const uint32_t rec0 = smem_addr(lrec);
         for (int e = r * E / C + threadIdx.x; e < e1; e += blockDim.x) {
