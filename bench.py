@@ -98,8 +98,9 @@ def hbm_peak() -> tuple[float, str]:
 
 
 # the sources of the decode call whose DRAM traffic profiles/ncu_traffic.json records
-DECODE_SOURCES = ("decode_kernel.cuh", "decode_streamk.cu", "decode_cluster.cu", "combine.cu",
-                  "merge.cuh", "streamk.h", "ptx.cuh", "dattn_internal.h", "dattn_api.cpp")
+DECODE_SOURCES = ("decode_kernel.cuh", "decode_streamk.cu", "decode_cluster.cu",
+                  "decode_cluster_paged.cu", "combine.cu", "merge.cuh", "streamk.h", "ptx.cuh",
+                  "dattn_internal.h", "dattn_api.cpp")
 
 
 def _code_only(text: str) -> str:
@@ -299,8 +300,13 @@ class Replica:
         self.outs = [torch.empty((w.batch, w.n_heads, w.head_dim), dtype=torch.float16,
                                  device=device) for _ in range(self.sets_n)]
         self.partitions = partitions
-        self.plan = dattn.dattn_decode_plan(w.batch, w.n_heads, w.head_dim, w.seq_len,
-                                            partitions)
+        if page_size:
+            pages = int(base["k"].shape[0])
+            self.plan = dattn.dattn_decode_paged_plan(w.batch, w.n_heads, w.head_dim, page_size,
+                                                      w.seq_len // page_size, pages, partitions)
+        else:
+            self.plan = dattn.dattn_decode_plan(w.batch, w.n_heads, w.head_dim, w.seq_len,
+                                                partitions)
         # enough for the dense and the paged call of this shape
         nbytes = max(16, dattn.dattn_decode_workspace_bytes(w.batch, w.n_heads, w.head_dim,
                                                             w.seq_len, partitions))
@@ -678,6 +684,7 @@ def sweep(device, stream, l2_bytes: int, steps: int, warmup: int, peak: float) -
     res = {}
     runs = [(n, 0) for n in ("small", "7b", "ragged", "long", "outlier")]
     runs += [(n, 16) for n in ("7b", "ragged", "long", "outlier")]
+    runs += [("7b", 128)]  # pages large enough for the cluster plan
     for name, ps in runs:
         key = name if not ps else f"{name}_paged{ps}"
         try:
@@ -690,12 +697,8 @@ def sweep(device, stream, l2_bytes: int, steps: int, warmup: int, peak: float) -
                          "frac_of_nominal_8TBs": gbs / NOMINAL_HBM_GBS,
                          "query_heads_per_s": r.w.batch * r.w.n_heads / t,
                          "isolated_step_us_p10_p50_p90": [pct["p10"], pct["p50"], pct["p90"]],
-                         # a paged cache always takes the split plan, whose partition
-                         # count the dense plan query does not report when the dense
-                         # shape takes the cluster plan
-                         "plan": ("cluster" if r.plan["cluster_size"] and not ps else "split"),
-                         "partitions": (r.plan["partitions"]
-                                        if not (ps and r.plan["cluster_size"]) else None),
+                         "plan": "cluster" if r.plan["cluster_size"] else "split",
+                         "partitions": r.plan["partitions"],
                          "algorithmic_bytes": r.bytes_per_step, "l2": r.l2_note}
             del r
         except Exception as e:  # report, keep going

@@ -94,11 +94,11 @@ const char *dattn_last_error(void);
  * `partitions` equal ranges, one per CTA, so every CTA streams the same number
  * of KV bytes whatever the mix of sequence lengths; a sequence whose positions
  * span several ranges is finished by a merge kernel.  The cluster plan (a
- * dense cache of a single sequence, library-chosen partitions): one
+ * single sequence, dense or paged cache, library-chosen partitions): one
  * thread-block cluster of `cluster_size` CTAs per (sequence, head group); the
- * CTAs of a cluster split the live positions and merge their partial softmax
- * states through distributed shared memory, so one launch writes `out` and no
- * workspace is used.
+ * CTAs of a cluster split the live positions (at page boundaries for a paged
+ * cache) and merge their partial softmax states through distributed shared
+ * memory, so one launch writes `out` and no workspace is used.
  */
 typedef struct dattn_plan {
     int partitions;      /* CTAs of the decode grid (equal ranges of positions)  */
@@ -124,6 +124,16 @@ typedef struct dattn_plan {
  */
 int dattn_decode_plan(int batch, int n_heads, int head_dim, int seq_len, int num_partitions,
                       dattn_plan *plan);
+
+/*
+ * The plan of dattn_decode_paged_f16 for (batch, n_heads, head_dim) over a pool
+ * of num_pages pages of page_size positions with max_pages table entries per
+ * sequence (seq_len = page_size * max_pages).  Same fields as dattn_decode_plan.
+ * Errors: as dattn_decode_plan, plus INVALID_ARG for non-positive page_size,
+ * max_pages or num_pages and UNSUPPORTED when page_size * max_pages >= 2^31.
+ */
+int dattn_decode_paged_plan(int batch, int n_heads, int head_dim, int page_size, int max_pages,
+                            long long num_pages, int num_partitions, dattn_plan *plan);
 
 /*
  * Workspace that dattn_decode_f16_ex and dattn_decode_paged_f16 need for this
@@ -191,8 +201,10 @@ int dattn_decode_f16(const void *Q, const void *K_cache, const void *V_cache, vo
  * Fused decode attention over a paged KV cache (the "direct page reads" form of
  * decode attention in "Tutorial 16: Writing Custom Metal Kernels", section 7,
  * for a cache held in fixed-size pages as the page-1 engine's paged block
- * allocator does).  Same operation, output and rounding as dattn_decode_f16_ex;
- * only the addressing of K and V differs:
+ * allocator does).  Same operation and output as dattn_decode_f16_ex; only the
+ * addressing of K and V differs (and, for a single sequence, possibly the plan:
+ * dattn_decode_paged_plan() reports it; where both calls take the same plan
+ * the rounding is the same too):
  *
  *   K_pages, V_pages  [num_pages, page_size, n_heads, head_dim]   f16, device
  *   block_table       [batch, max_pages]                          int32, device
@@ -205,9 +217,9 @@ int dattn_decode_f16(const void *Q, const void *K_cache, const void *V_cache, vo
  * prefetch hints before the kernel before it on `stream` has finished; such a
  * hint is bounds-checked and changes no result.)  A live entry outside
  * [0, num_pages) is not dereferenced: page 0 is read instead, the output of
- * that call is wrong, and dattn_device_error() reports DATTN_ERR_BAD_PAGE.  The workspace is the one of
- * dattn_decode_workspace_bytes(batch, n_heads, head_dim, page_size * max_pages,
- * num_partitions).
+ * that call is wrong, and dattn_device_error() reports DATTN_ERR_BAD_PAGE.
+ * The workspace is the one of dattn_decode_workspace_bytes(batch, n_heads,
+ * head_dim, page_size * max_pages, num_partitions).
  * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA.
  */
 int dattn_decode_paged_f16(const void *Q, const void *K_pages, const void *V_pages, void *out,

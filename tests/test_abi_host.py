@@ -109,6 +109,16 @@ def test_plan_queries_reject_bad_arguments_on_host(lib):
     assert lib.dattn_decode_workspace_bytes(1, 2, 63, 16, 0, ctypes.byref(n)) == \
         _native.ERR_UNSUPPORTED
     assert lib.dattn_decode_plan(1, 2, 64, 16, 0, None) == _native.ERR_INVALID_ARG
+    plan = _native.Plan()
+    assert lib.dattn_decode_paged_plan(1, 2, 64, 16, 4, 10, 0, None) == _native.ERR_INVALID_ARG
+    assert lib.dattn_decode_paged_plan(1, 2, 64, 0, 4, 10, 0, ctypes.byref(plan)) == \
+        _native.ERR_INVALID_ARG
+    assert lib.dattn_decode_paged_plan(1, 2, 64, 16, 4, 0, 0, ctypes.byref(plan)) == \
+        _native.ERR_INVALID_ARG
+    assert lib.dattn_decode_paged_plan(1, 2, 64, 1 << 20, 1 << 12, 10, 0, ctypes.byref(plan)) == \
+        _native.ERR_UNSUPPORTED
+    assert lib.dattn_decode_paged_plan(1, 2, 63, 16, 4, 10, 0, ctypes.byref(plan)) == \
+        _native.ERR_UNSUPPORTED
 
 
 def test_python_binding_rejects_pageable_cpu_tensors():

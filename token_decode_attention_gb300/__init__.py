@@ -13,6 +13,7 @@ from ._native import (  # noqa: F401
     dattn_decode_f16,
     dattn_decode_f16_ex,
     dattn_decode_paged_f16,
+    dattn_decode_paged_plan,
     dattn_decode_plan,
     dattn_decode_workspace_bytes,
     dattn_device_error,

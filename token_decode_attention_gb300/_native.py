@@ -49,6 +49,8 @@ _SIGNATURES = {
     "dattn_status_string": ([_I], ctypes.c_char_p),
     "dattn_last_error": ([], ctypes.c_char_p),
     "dattn_decode_plan": ([_I, _I, _I, _I, _I, ctypes.POINTER(Plan)], _I),
+    "dattn_decode_paged_plan": ([_I, _I, _I, _I, _I, ctypes.c_longlong, _I, ctypes.POINTER(Plan)],
+                                _I),
     "dattn_decode_workspace_bytes": ([_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)], _I),
     "dattn_decode_f16_ex": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, ctypes.c_size_t, _I, _P],
                             _I),
@@ -154,6 +156,15 @@ def dattn_decode_plan(batch: int, n_heads: int, head_dim: int, seq_len: int,
     plan = Plan()
     _check(load().dattn_decode_plan(batch, n_heads, head_dim, seq_len, num_partitions,
                                     ctypes.byref(plan)), "dattn_decode_plan")
+    return plan.as_dict()
+
+
+def dattn_decode_paged_plan(batch: int, n_heads: int, head_dim: int, page_size: int,
+                            max_pages: int, num_pages: int, num_partitions: int = 0) -> dict:
+    plan = Plan()
+    _check(load().dattn_decode_paged_plan(batch, n_heads, head_dim, page_size, max_pages,
+                                          num_pages, num_partitions, ctypes.byref(plan)),
+           "dattn_decode_paged_plan")
     return plan.as_dict()
 
 

@@ -18,8 +18,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdattn.so")
-SOURCES = ["decode_streamk.cu", "decode_cluster.cu", "combine.cu", "split_calls.cu",
-           "decode_noalloc.cu", "selftest.cu", "softmax.cu", "rope_append.cu", "dattn_api.cpp"]
+SOURCES = ["decode_streamk.cu", "decode_cluster.cu", "decode_cluster_paged.cu", "combine.cu",
+           "split_calls.cu", "decode_noalloc.cu", "selftest.cu", "softmax.cu", "rope_append.cu",
+           "dattn_api.cpp"]
 HEADERS = ["dattn_internal.h", "ptx.cuh", "streamk.h", "merge.cuh", "decode_kernel.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -76,6 +76,16 @@ constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
 #ifndef DATTN_CLUSTER_MAX_CAPACITY_BYTES
 #define DATTN_CLUSTER_MAX_CAPACITY_BYTES (512LL << 20)  // K+V capacity up to which it is used
 #endif
+#ifndef DATTN_CLUSTER_PAGED_MIN_COPY_BYTES
+// A paged cache takes the cluster plan only when one page of a head group (one
+// tensor box or bulk copy) holds at least this much K, and only with as many
+// CTAs as the plan of a dense cache of the same shape.  The copies are issued
+// one per page; on GB300 a 7B-class step (128 CTAs of one head, 256 B rows)
+// measured 30.6 us with 4 KB page boxes (16-position pages), 15.5 us with
+// 16 KB and 14.9 us with 32 KB, and 64 CTAs of 8 heads (32 KB boxes of
+// 16-position pages) 21.7 us, against 15.3-15.5 us for the split plan.
+#define DATTN_CLUSTER_PAGED_MIN_COPY_BYTES (32 * 1024)
+#endif
 #ifndef DATTN_CLUSTER_MAX_SIZE
 #define DATTN_CLUSTER_MAX_SIZE 16  // CTAs per cluster (8 is the portable limit)
 #endif
@@ -168,7 +178,7 @@ struct Plan {
     int combine_chunk = 0;  // channels per combine CTA
     int combine_inflight = 8;  // piece loads per combine thread per round
     // cluster mode (see DecodeArgs::cluster): CTAs per cluster (0 = stream-K)
-    int cluster = 0, use_tmap = 0, rec_offset = 0;
+    int cluster = 0, use_tmap = 0, rec_offset = 0, box_pos = 0;
 };
 
 int next_pow2(int x) {
@@ -195,7 +205,8 @@ int validate_dims(int B, int H, int D, int S) {
     return DATTN_OK;
 }
 
-using PlanKey = std::tuple<int, int, int, int, int, int, bool>;
+// (device, B, H, D, S, num_partitions, page_size: 0 dense, -1 paged of any page size)
+using PlanKey = std::tuple<int, int, int, int, int, int, int>;
 std::mutex g_plan_mutex;
 std::map<PlanKey, Plan> g_plans;
 
@@ -218,7 +229,17 @@ int choose_partitions(const Plan &p, int B, int S) {
     return static_cast<int>(std::min<long long>({slots, by_work, kMaxPartitions}));
 }
 
-int make_cluster_plan(int B, int H, int D, int S, const DeviceInfo &di, Plan *out);
+int make_cluster_plan(int B, int H, int D, int S, int page_size, const DeviceInfo &di, Plan *out);
+
+int lcm_int(int x, int y) {
+    int a = x, b = y;
+    while (b != 0) {
+        const int t = a % b;
+        a = b;
+        b = t;
+    }
+    return x / a * y;
+}
 
 // The split (stream-K) plan with at least `min_groups` head groups.
 int split_plan(int B, int H, int D, int S, int num_partitions, int min_groups,
@@ -323,7 +344,10 @@ int split_plan(int B, int H, int D, int S, int num_partitions, int min_groups,
 }
 
 
-int make_plan(int B, int H, int D, int S, int num_partitions, bool paged, Plan *out) {
+// page_size: 0 for a dense cache, the page size of a paged one, or -1 for a
+// paged cache whose page size is not known (the split plan, which any paged
+// call can run).
+int make_plan(int B, int H, int D, int S, int num_partitions, int page_size, Plan *out) {
     if (int st = validate_dims(B, H, D, S)) return st;
     if (num_partitions < 0)
         return fail(DATTN_ERR_INVALID_ARG, "num_partitions=%d must be >= 0", num_partitions);
@@ -331,7 +355,7 @@ int make_plan(int B, int H, int D, int S, int num_partitions, bool paged, Plan *
     if (int st = device_info(&di)) return st;
     int dev = 0;
     if (int st = current_device(&dev)) return st;
-    const PlanKey key{dev, B, H, D, S, num_partitions, paged};
+    const PlanKey key{dev, B, H, D, S, num_partitions, page_size};
     {
         std::lock_guard<std::mutex> lock(g_plan_mutex);
         auto it = g_plans.find(key);
@@ -345,9 +369,15 @@ int make_plan(int B, int H, int D, int S, int num_partitions, bool paged, Plan *
     // Few sequences (dense cache, library-chosen partitions): one cluster of
     // CTAs per (sequence, head group), merged in distributed shared memory,
     // when such a plan exists.
-    if (num_partitions == 0 && !paged && B <= kClusterMaxBatch) {
+    if (num_partitions == 0 && page_size >= 0 && B <= kClusterMaxBatch) {
         Plan c;
-        if (int st = make_cluster_plan(B, H, D, S, di, &c)) return st;
+        if (int st = make_cluster_plan(B, H, D, S, page_size, di, &c)) return st;
+        if (c.cluster > 0 && page_size > 0) {
+            // a paged cache keeps the dense plan's parallelism or takes the split plan
+            Plan d;
+            if (int st = make_cluster_plan(B, H, D, S, 0, di, &d)) return st;
+            if (c.G < d.G) c.cluster = 0;
+        }
         if (c.cluster > 0) p = c;
     }
     {
@@ -364,11 +394,13 @@ int make_plan(int B, int H, int D, int S, int num_partitions, bool paged, Plan *
 // B * NHG clusters fit on the GPU at once, take the one with the most CTAs
 // while each CTA still holds DATTN_CLUSTER_MIN_CTA_BYTES of K+V capacity; on a
 // tie, fewer head groups (longer rows).  out->cluster stays 0 when none fits.
-int make_cluster_plan(int B, int H, int D, int S, const DeviceInfo &di, Plan *out) {
+int make_cluster_plan(int B, int H, int D, int S, int page_size, const DeviceInfo &di, Plan *out) {
     *out = Plan();
     const double cap_bytes = 4.0 * B * static_cast<double>(S) * H * D;  // K + V
     if (cap_bytes > static_cast<double>(DATTN_CLUSTER_MAX_CAPACITY_BYTES)) return DATTN_OK;
-    if (static_cast<double>(B) * S >= 2147483647.0) return DATTN_OK;  // 32-bit box coordinate
+    // 32-bit box coordinate (a paged caller checks the rows of its pool)
+    if (page_size == 0 && static_cast<double>(B) * S >= 2147483647.0) return DATTN_OK;
+    if (page_size < 0) return DATTN_OK;
     const int c8 = D / 8;
     int bdx, ch;
     if (c8 <= 8) {
@@ -408,16 +440,24 @@ int make_cluster_plan(int B, int H, int D, int S, const DeviceInfo &di, Plan *ou
             if (ctas > static_cast<long long>(di.sms)) continue;
             if (C > 1 && cap_bytes / static_cast<double>(ctas) < DATTN_CLUSTER_MIN_CTA_BYTES) continue;
             // a stage: ~DATTN_CLUSTER_STAGE_BYTES of K+V, no more than a CTA's
-            // share of the capacity, a multiple of the phases
+            // share of the capacity, a multiple of the phases (and of the page
+            // size: the CTAs' ranges start on a page, so do the stages)
+            const int quantum = page_size > 0 ? lcm_int(p.PHI, page_size) : p.PHI;
+            if (quantum > 256) continue;
             const int share = (S + C - 1) / C;
             int P = std::max(1, std::min(256, DATTN_CLUSTER_STAGE_BYTES / 2 / row_bytes));
-            P = std::min(P, std::max(share, p.PHI));
-            P = std::max(p.PHI, P / p.PHI * p.PHI);
+            P = std::min(P, std::max(share, quantum));
+            P = std::max(quantum, P / quantum * quantum);
             if (P > 256) continue;
-            // a head group's rows are copied as one tensor box {D, HG, P} per full stage
-            // (the box's shared-memory destination is 128-byte aligned)
+            // a head group's rows are copied as tensor boxes {D, HG, box}: a full
+            // stage of a dense cache, a whole page of a paged one (the box's
+            // shared-memory destination is 128-byte aligned)
             const bool grouped = hg < H;
-            if (grouped && (static_cast<long long>(P) * row_bytes) % 128 != 0) continue;
+            const int box = page_size > 0 ? page_size : P;
+            if (grouped && (static_cast<long long>(box) * row_bytes) % 128 != 0) continue;
+            if (page_size > 0 &&
+                static_cast<long long>(page_size) * row_bytes < DATTN_CLUSTER_PAGED_MIN_COPY_BYTES)
+                continue;
             const int merge_bytes = p.PHI > 1 ? hg * p.PHI * (D + 2) * 4 : 0;
             const int rec_bytes = hg * (D + 2) * 4;  // the CTA's record (m, l, acc) per head
             const int stage_bytes = 2 * P * row_bytes;
@@ -434,7 +474,7 @@ int make_cluster_plan(int B, int H, int D, int S, const DeviceInfo &di, Plan *ou
             q.smem = q.bar_offset + nst * 16 + 16;
             if (q.smem > di.max_smem_optin - kStaticSmemReserve) continue;
             int clusters = 0;
-            cudaError_t e = dattn::decode_max_clusters(q.v, q.smem, C, &clusters);
+            cudaError_t e = dattn::decode_max_clusters(q.v, q.smem, C, page_size > 0, &clusters);
             if (e != cudaSuccess) {
                 cudaGetLastError();  // this cluster size is not available: try the next
                 continue;
@@ -447,6 +487,7 @@ int make_cluster_plan(int B, int H, int D, int S, const DeviceInfo &di, Plan *ou
             if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
             q.cluster = C;
             q.use_tmap = grouped ? 1 : 0;
+            q.box_pos = box;
             q.G = static_cast<int>(ctas);
             q.ws_bytes = 0;
             best = q;
@@ -491,17 +532,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// Tensor map of a dense cache [B*S positions, H heads, D] (f16, innermost D)
-// whose box is one stage of one head group: {D, HG, P}.
-int encode_kv_box(CUtensorMap *map, const void *base, int B, int H, int D, int S, int HG, int P) {
+// Tensor map of a cache [rows, H heads, D] (f16, innermost D) whose box is
+// `box_rows` rows of one head group, {D, HG, box_rows}: the B*S positions of a
+// dense cache and one stage, or the num_pages*page_size rows of a page pool
+// and one page.
+int encode_kv_box(CUtensorMap *map, const void *base, long long rows, int H, int D, int HG,
+                  int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr) return fail(DATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
-                                static_cast<cuuint64_t>(B) * static_cast<cuuint64_t>(S)};
+                                static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                                    static_cast<cuuint64_t>(H) * D * 2};  // bytes, dims 1 and 2
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(HG),
-                               static_cast<cuuint32_t>(P)};
+                               static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t unit[3] = {1, 1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims,
                            strides, box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -552,9 +596,12 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
     a.cluster = p.cluster;
     a.use_tmap = p.use_tmap;
     a.rec_offset = p.rec_offset;
+    a.box_pos = p.box_pos;
     if (p.use_tmap) {
-        if (int st = encode_kv_box(&a.tmap_k, K, B, H, D, S, p.HG, p.P)) return st;
-        if (int st = encode_kv_box(&a.tmap_v, V, B, H, D, S, p.HG, p.P)) return st;
+        const long long rows = pg.table != nullptr ? pg.num_pages * pg.page_size
+                                                   : static_cast<long long>(B) * S;
+        if (int st = encode_kv_box(&a.tmap_k, K, rows, H, D, p.HG, p.box_pos)) return st;
+        if (int st = encode_kv_box(&a.tmap_v, V, rows, H, D, p.HG, p.box_pos)) return st;
     }
     cudaError_t e = dattn::launch_decode(a, p.v, p.smem, stream);
     if (e != cudaSuccess) return fail_cuda(e, "decode kernel launch");
@@ -615,11 +662,8 @@ const char *dattn_status_string(int status) {
 
 const char *dattn_last_error(void) { return g_last_error.c_str(); }
 
-int dattn_decode_plan(int batch, int n_heads, int head_dim, int seq_len, int num_partitions,
-                      dattn_plan *plan) {
-    if (plan == nullptr) return fail(DATTN_ERR_INVALID_ARG, "plan is NULL");
-    Plan p;
-    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, false, &p)) return st;
+namespace {
+void fill_plan(const Plan &p, dattn_plan *plan) {
     plan->partitions = p.G;
     plan->heads_per_cta = p.HG;
     plan->head_groups = p.NHG;
@@ -631,17 +675,54 @@ int dattn_decode_plan(int batch, int n_heads, int head_dim, int seq_len, int num
     plan->sm_count = p.sms;
     plan->workspace_bytes = p.ws_bytes;
     plan->cluster_size = p.cluster;
+}
+
+// The paged call's plan key: its page size, or -1 (the split plan) when the
+// pool's rows do not fit the 32-bit row coordinate of a tensor box.
+int paged_plan(int batch, int n_heads, int head_dim, int page_size, int max_pages,
+               long long num_pages, int num_partitions, Plan *p) {
+    if (page_size <= 0 || max_pages <= 0 || num_pages <= 0)
+        return fail(DATTN_ERR_INVALID_ARG,
+                    "page_size=%d, max_pages=%d and num_pages=%lld must be positive", page_size,
+                    max_pages, num_pages);
+    const long long cap = static_cast<long long>(page_size) * max_pages;
+    if (cap > 0x7fffffffLL)
+        return fail(DATTN_ERR_UNSUPPORTED, "page_size x max_pages = %lld exceeds 2^31 - 1", cap);
+    const bool box_rows_ok = static_cast<double>(num_pages) * page_size < 2147483647.0;
+    return make_plan(batch, n_heads, head_dim, static_cast<int>(cap), num_partitions,
+                     box_rows_ok ? page_size : -1, p);
+}
+}  // namespace
+
+int dattn_decode_plan(int batch, int n_heads, int head_dim, int seq_len, int num_partitions,
+                      dattn_plan *plan) {
+    if (plan == nullptr) return fail(DATTN_ERR_INVALID_ARG, "plan is NULL");
+    Plan p;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, 0, &p)) return st;
+    fill_plan(p, plan);
+    return DATTN_OK;
+}
+
+int dattn_decode_paged_plan(int batch, int n_heads, int head_dim, int page_size, int max_pages,
+                            long long num_pages, int num_partitions, dattn_plan *plan) {
+    if (plan == nullptr) return fail(DATTN_ERR_INVALID_ARG, "plan is NULL");
+    Plan p;
+    if (int st = paged_plan(batch, n_heads, head_dim, page_size, max_pages, num_pages,
+                            num_partitions, &p))
+        return st;
+    fill_plan(p, plan);
     return DATTN_OK;
 }
 
 int dattn_decode_workspace_bytes(int batch, int n_heads, int head_dim, int seq_len,
                                  int num_partitions, size_t *bytes) {
     if (bytes == nullptr) return fail(DATTN_ERR_INVALID_ARG, "bytes is NULL");
-    // enough for the dense call and for the paged call of the same capacity
-    // (a dense cache of few sequences may take the cluster plan, which needs none)
+    // enough for the dense call and for the paged call of the same capacity and
+    // any page size (a cache of few sequences may take the cluster plan, which
+    // needs none; the split plan covers every paged call)
     Plan p, q;
-    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, false, &p)) return st;
-    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, true, &q)) return st;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, 0, &p)) return st;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, -1, &q)) return st;
     *bytes = std::max(p.ws_bytes, q.ws_bytes);
     return DATTN_OK;
 }
@@ -659,7 +740,7 @@ int dattn_decode_f16_ex(const void *Q, const void *K_cache, const void *V_cache,
     if (num_partitions < 0)
         return fail(DATTN_ERR_INVALID_ARG, "num_partitions=%d must be >= 0", num_partitions);
     Plan p;
-    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, false, &p)) return st;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, num_partitions, 0, &p)) return st;
     if (p.ws_bytes > 0) {
         if (workspace == nullptr)
             return fail(DATTN_ERR_WORKSPACE, "workspace of %zu bytes required, got NULL",
@@ -683,7 +764,7 @@ int dattn_decode_f16(const void *Q, const void *K_cache, const void *V_cache, vo
     if (int st = check_tensor(out, "out")) return st;
     if (int st = check_cur_pos(current_pos)) return st;
     Plan p;
-    if (int st = make_plan(batch, n_heads, head_dim, seq_len, 0, false, &p)) return st;
+    if (int st = make_plan(batch, n_heads, head_dim, seq_len, 0, 0, &p)) return st;
     void *ws = nullptr;
     if (p.ws_bytes > 0) {
         int dev = 0;
@@ -742,7 +823,9 @@ int dattn_decode_paged_f16(const void *Q, const void *K_pages, const void *V_pag
     if (num_partitions < 0)
         return fail(DATTN_ERR_INVALID_ARG, "num_partitions=%d must be >= 0", num_partitions);
     Plan p;
-    if (int st = make_plan(batch, n_heads, head_dim, S, num_partitions, true, &p)) return st;
+    if (int st = paged_plan(batch, n_heads, head_dim, page_size, max_pages, num_pages,
+                            num_partitions, &p))
+        return st;
     if (p.ws_bytes > 0) {
         if (workspace == nullptr)
             return fail(DATTN_ERR_WORKSPACE, "workspace of %zu bytes required, got NULL",

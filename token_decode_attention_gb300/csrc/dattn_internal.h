@@ -36,8 +36,9 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // one second
 // the others.
 struct DecodeArgs {
     // Cluster mode (cluster > 0) with a head group smaller than H: tiled tensor
-    // maps of K and V as [B*S positions, H, D] (innermost D), box {D, HG, P}.
-    // One box is one full stage of a head group.
+    // maps of K and V as [rows, H, D] (innermost D), box {D, HG, box_pos}: for a
+    // dense cache the B*S positions and one full stage of a head group, for a
+    // paged cache the num_pages*page_size rows of the pool and one page.
     CUtensorMap tmap_k, tmap_v;
     const void *Q;            // f16 [B,H,D]
     const void *K;            // f16 [B,S,H,D]
@@ -75,7 +76,8 @@ struct DecodeArgs {
     // the C partial states are merged through distributed shared memory into
     // `out`.  No workspace and no second kernel.
     int cluster;
-    int use_tmap;      // full stages of a head group are copied as one tensor box
+    int use_tmap;      // full stages (pages) of a head group are copied as tensor boxes
+    int box_pos;       // positions of a tensor box: a stage (dense) or a page (paged)
     // Cluster mode: byte offset of this CTA's record [HG][D + 2] of its
     // partial state (m, l, acc) per head, read by the cluster's other CTAs.
     int rec_offset;
@@ -109,7 +111,7 @@ cudaError_t launch_decode(const DecodeArgs &a, DecodeVariant v, int smem, cudaSt
 // Resident CTAs per SM for a variant at a given dynamic shared memory size.
 cudaError_t decode_occupancy(DecodeVariant v, int smem, int *ctas_per_sm);
 // Clusters of `cluster` CTAs of a variant that can be resident at once.
-cudaError_t decode_max_clusters(DecodeVariant v, int smem, int cluster, int *clusters);
+cudaError_t decode_max_clusters(DecodeVariant v, int smem, int cluster, bool paged, int *clusters);
 // Raise the dynamic shared memory limit of every variant (once per device).
 cudaError_t decode_configure_smem(int max_smem);
 // Launch the combine kernel with programmatic dependent launch on `stream`.

@@ -1,8 +1,9 @@
 // decode_kernel.cuh -- the fused decode-attention kernel template for sm_103a,
 // instantiated for the split plan (dense and paged caches) in decode_streamk.cu
-// and for the cluster plan (dense caches) in decode_cluster.cu: two
-// translation units, built in parallel, each instance holding only its own
-// plan's code, which keeps the latency-bound launches of either plan lean.
+// and for the cluster plan in decode_cluster.cu (dense caches) and
+// decode_cluster_paged.cu (paged caches): translation units built in parallel,
+// each instance holding only its own mode's code, which keeps the
+// latency-bound launches of every mode lean.
 // (Separate dense and paged instances of the split plan were measured too:
 // the dense one ran long 1.3 % slower, so the split plan keeps one.)
 //
@@ -169,9 +170,17 @@ __device__ __forceinline__ bool next_piece(Walker &w, const DecodeArgs &a) {
     return true;
 }
 
-template <int BDX, int CH, int KMAX, int NWC, bool CLUSTER>
+// Instance modes: the split plan (dense and paged caches), the cluster plan
+// over a dense cache, the cluster plan over a paged cache.  Each instance
+// holds only its mode's code: on latency-bound launches the unused code of
+// another mode measured up to 1.8 us per call.
+constexpr int kModeSplit = 0, kModeCluster = 1, kModeClusterPaged = 2;
+
+template <int BDX, int CH, int KMAX, int NWC, int MODE>
 __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     decode_streamk_kernel(const __grid_constant__ DecodeArgs a) {
+    constexpr bool CLUSTER = MODE != kModeSplit;
+    constexpr bool PAGED_OK = MODE != kModeCluster;  // the dense cluster instances have no paging
     constexpr int NPOS = 2;              // positions per (head, phase) slot in a consumer group
     constexpr int BDY = 32 / BDX;        // lane groups per warp
     constexpr int NLG = NWC * BDY;       // lane groups per CTA
@@ -224,7 +233,9 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         if constexpr (CLUSTER) {  // CTA r of cluster u: [r S / C, (r+1) S / C) of unit u
             const long long u = blockIdx.x / a.cluster;
             const long long r = blockIdx.x - u * a.cluster;
-            x = u * S + r * S / a.cluster;
+            long long r0 = r * S / a.cluster;
+            if constexpr (MODE == kModeClusterPaged) r0 -= r0 % a.page_size;  // ranges start on a page
+            x = u * S + r0;
             x_lim = u * S + (r + 1) * S / a.cluster;
         } else {
             x = static_cast<long long>(blockIdx.x) * Wc / a.partitions;
@@ -241,7 +252,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
             long long n = min(S - off, x_end - x);
             long long first_pos = b * S + off;  // dense: row index in [B*S]
             bool go = true;
-            if (!CLUSTER && a.block_table != nullptr) {  // the cluster plan is dense only
+            if (PAGED_OK && a.block_table != nullptr) {
                 const long long pidx = off / a.page_size;
                 const long long in_page = off - pidx * a.page_size;
                 n = min(n, static_cast<long long>(a.page_size) - in_page);
@@ -257,8 +268,8 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                     const uint32_t bytes = static_cast<uint32_t>(n * row * 2);
                     bulk_prefetch_l2(k0, bytes);
                     bulk_prefetch_l2(v0, bytes);
-                } else if (CLUSTER && a.use_tmap) {  // a head group: whole tensor boxes of P positions
-                    for (long long j = 0; j + a.stage_pos <= n; j += a.stage_pos) {
+                } else if (CLUSTER && a.use_tmap) {  // a head group: whole tensor boxes
+                    for (long long j = 0; j + a.box_pos <= n; j += a.box_pos) {
                         const int row0 = static_cast<int>(first_pos + j);
                         tensor3d_prefetch_l2(&a.tmap_k, 0, h0, row0);
                         tensor3d_prefetch_l2(&a.tmap_v, 0, h0, row0);
@@ -302,8 +313,15 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         b0 = u / nhg;
         L0 = live_len(a.cur_pos, b0, a.S);
         const long long g = u - b0 * nhg;
-        x0 = g * L0 + r * L0 / a.cluster;
-        x1 = g * L0 + (r + 1) * L0 / a.cluster;
+        long long r0 = r * L0 / a.cluster, r1 = (r + 1) * L0 / a.cluster;
+        if constexpr (MODE == kModeClusterPaged) {
+            // ranges start on a page, so every stage is whole pages (one tensor
+            // box each) but for the unit's last page
+            r0 -= r0 % a.page_size;
+            r1 = r + 1 == a.cluster ? L0 : r1 - r1 % a.page_size;
+        }
+        x0 = g * L0 + r0;
+        x1 = g * L0 + r1;
         base0 = 0;
     } else if (a.B <= 32) {
         // Lane b holds sequence b: every warp scans the batch on its own, with
@@ -473,7 +491,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         // ---------------- producer warp ----------------
         const uint64_t policy = l2_evict_first_policy();
         const size_t pos_stride = static_cast<size_t>(a.H) * D;  // halves between positions
-        const bool paged = !CLUSTER && a.block_table != nullptr;  // the cluster plan is dense only
+        const bool paged = PAGED_OK && a.block_table != nullptr;
         // tensor boxes need a 128-byte aligned destination; otherwise the
         // per-position copies below serve (same data, more copies)
         const bool tmap_ok = CLUSTER && a.use_tmap && (smem_addr(smem) & 127u) == 0;
@@ -521,7 +539,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                             bulk_g2s(dK, sK, np * row_bytes, &full_bar[slot], policy);
                             bulk_g2s(dV, sV, np * row_bytes, &full_bar[slot], policy);
                         }
-                    } else if (tmap_ok && np == a.stage_pos) {
+                    } else if (tmap_ok && np == a.box_pos) {
                         // a full stage of the head group: one tensor box each
                         // ({D, HG, P} at row b*S + pos0; the host checked that
                         // B*S fits the 32-bit coordinate)
@@ -566,6 +584,14 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                             if (lane == 0) {
                                 bulk_g2s(tK, sK, run * row_bytes, &full_bar[slot], policy);
                                 bulk_g2s(tV, sV, run * row_bytes, &full_bar[slot], policy);
+                            }
+                        } else if (tmap_ok && run == a.box_pos) {
+                            // a whole page of the head group: one tensor box each
+                            // ({D, HG, page_size} at row page * page_size of the pool)
+                            if (lane == 0) {
+                                const int row0 = static_cast<int>(page * a.page_size);
+                                tensor3d_g2s(tK, &a.tmap_k, 0, h0, row0, &full_bar[slot], policy);
+                                tensor3d_g2s(tV, &a.tmap_v, 0, h0, row0, &full_bar[slot], policy);
                             }
                         } else {
                             for (int r = lane; r < run; r += 32) {
@@ -898,33 +924,33 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
 // warps.  Eight consumer warps (two CTAs per SM) up to one slot of two chunks
 // or two slots of one chunk per lane group; sixteen consumer warps (one CTA per
 // SM, the same warps per SM) when a CTA must hold more heads.
-template <int BDX, int CH, int NWC, bool CLUSTER>
+template <int BDX, int CH, int NWC, int MODE>
 const void *pick_kmax(int kmax) {
     switch (kmax) {
-        case 1: return reinterpret_cast<const void *>(decode_streamk_kernel<BDX, CH, 1, NWC, CLUSTER>);
+        case 1: return reinterpret_cast<const void *>(decode_streamk_kernel<BDX, CH, 1, NWC, MODE>);
         case 2:
             if constexpr (CH == 1)
-                return reinterpret_cast<const void *>(decode_streamk_kernel<BDX, CH, 2, NWC, CLUSTER>);
+                return reinterpret_cast<const void *>(decode_streamk_kernel<BDX, CH, 2, NWC, MODE>);
             return nullptr;
         default: return nullptr;
     }
 }
 
-template <int NWC, bool CLUSTER>
+template <int NWC, int MODE>
 const void *pick_shape(int bdx, int ch, int kmax) {
     if (ch == 1) {
         switch (bdx) {
-            case 1: return pick_kmax<1, 1, NWC, CLUSTER>(kmax);
-            case 2: return pick_kmax<2, 1, NWC, CLUSTER>(kmax);
-            case 4: return pick_kmax<4, 1, NWC, CLUSTER>(kmax);
-            case 8: return pick_kmax<8, 1, NWC, CLUSTER>(kmax);
+            case 1: return pick_kmax<1, 1, NWC, MODE>(kmax);
+            case 2: return pick_kmax<2, 1, NWC, MODE>(kmax);
+            case 4: return pick_kmax<4, 1, NWC, MODE>(kmax);
+            case 8: return pick_kmax<8, 1, NWC, MODE>(kmax);
             default: return nullptr;
         }
     }
     if (ch == 2) {
         switch (bdx) {
-            case 8: return pick_kmax<8, 2, NWC, CLUSTER>(kmax);
-            case 16: return pick_kmax<16, 2, NWC, CLUSTER>(kmax);
+            case 8: return pick_kmax<8, 2, NWC, MODE>(kmax);
+            case 16: return pick_kmax<16, 2, NWC, MODE>(kmax);
             default: return nullptr;
         }
     }
@@ -932,10 +958,10 @@ const void *pick_shape(int bdx, int ch, int kmax) {
 }
 
 // The instances of one mode.
-template <bool CLUSTER>
+template <int MODE>
 const void *variant_fn_of(DecodeVariant v) {
-    if (v.nwc == 8) return pick_shape<8, CLUSTER>(v.bdx, v.ch, v.kmax);
-    if (v.nwc == 16) return pick_shape<16, CLUSTER>(v.bdx, v.ch, v.kmax);
+    if (v.nwc == 8) return pick_shape<8, MODE>(v.bdx, v.ch, v.kmax);
+    if (v.nwc == 16) return pick_shape<16, MODE>(v.bdx, v.ch, v.kmax);
     return nullptr;
 }
 

@@ -1,25 +1,34 @@
 // decode_streamk.cu -- launchers of the fused decode kernel
 // (decode_kernel.cuh) and the instances of its split (stream-K) plan.  The
-// cluster plan's instances are in decode_cluster.cu.
+// cluster plan's instances are in decode_cluster.cu (dense caches) and
+// decode_cluster_paged.cu (paged caches).
 #include "decode_kernel.cuh"
 
 namespace dattn {
 
 __device__ unsigned g_device_error = 0;
 
-// the cluster plan's instances (decode_cluster.cu)
+// the cluster plan's instances (decode_cluster.cu, decode_cluster_paged.cu)
 const void *decode_cluster_variant_fn(DecodeVariant v);
+const void *decode_cluster_paged_variant_fn(DecodeVariant v);
 
 namespace {
 
-const void *variant_fn(DecodeVariant v, bool cluster) {
-    return cluster ? decode_cluster_variant_fn(v) : variant_fn_of<false>(v);
+const void *variant_fn(DecodeVariant v, int mode) {
+    switch (mode) {
+        case kModeSplit: return variant_fn_of<kModeSplit>(v);
+        case kModeCluster: return decode_cluster_variant_fn(v);
+        case kModeClusterPaged: return decode_cluster_paged_variant_fn(v);
+        default: return nullptr;
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs &a, DecodeVariant v, int smem, cudaStream_t stream) {
-    const void *fn = variant_fn(v, a.cluster > 0);
+    const int mode = a.cluster == 0 ? kModeSplit
+                                    : (a.block_table != nullptr ? kModeClusterPaged : kModeCluster);
+    const void *fn = variant_fn(v, mode);
     if (fn == nullptr || a.partitions <= 0) return cudaErrorInvalidValue;
     void *args[] = {const_cast<DecodeArgs *>(&a)};
     cudaLaunchConfig_t cfg = {};
@@ -45,14 +54,14 @@ cudaError_t launch_decode(const DecodeArgs &a, DecodeVariant v, int smem, cudaSt
 }
 
 cudaError_t decode_occupancy(DecodeVariant v, int smem, int *ctas_per_sm) {
-    const void *fn = variant_fn(v, false);
+    const void *fn = variant_fn(v, kModeSplit);
     if (fn == nullptr) return cudaErrorInvalidValue;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, decode_threads(v.nwc),
                                                          static_cast<size_t>(smem));
 }
 
-cudaError_t decode_max_clusters(DecodeVariant v, int smem, int cluster, int *clusters) {
-    const void *fn = variant_fn(v, true);
+cudaError_t decode_max_clusters(DecodeVariant v, int smem, int cluster, bool paged, int *clusters) {
+    const void *fn = variant_fn(v, paged ? kModeClusterPaged : kModeCluster);
     if (fn == nullptr || cluster < 1 || cluster > kMaxCluster) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(cluster));
@@ -75,8 +84,8 @@ cudaError_t decode_configure_smem(int max_smem) {
         {1, 1, 1, 16}, {1, 1, 2, 16}, {2, 1, 1, 16}, {2, 1, 2, 16}, {4, 1, 1, 16},
         {4, 1, 2, 16}, {8, 1, 1, 16}, {8, 1, 2, 16}, {8, 2, 1, 16}, {16, 2, 1, 16}};
     for (const DecodeVariant &v : variants) {
-        for (const bool cluster : {false, true}) {
-            const void *fn = variant_fn(v, cluster);
+        for (const int mode : {kModeSplit, kModeCluster, kModeClusterPaged}) {
+            const void *fn = variant_fn(v, mode);
             // static and dynamic shared memory together may not exceed the opt-in limit
             cudaFuncAttributes attr{};
             cudaError_t e = cudaFuncGetAttributes(&attr, fn);
@@ -85,7 +94,7 @@ cudaError_t decode_configure_smem(int max_smem) {
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
             if (e != cudaSuccess) return e;
             // the cluster plan launches clusters of up to 16 CTAs
-            if (cluster)
+            if (mode != kModeSplit)
                 e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             if (e != cudaSuccess) return e;
         }
