@@ -210,3 +210,74 @@ def test_random_cases_cover_both_plans():
     plans = [dattn.dattn_decode_paged_plan(1, H, D, ps, maxp, maxp + 3)["cluster_size"] > 0
              for H, D, ps, maxp, _, _ in RANDOM_CASES]
     assert sum(plans) >= 12 and len(plans) - sum(plans) >= 12, sum(plans)
+
+
+def test_append_and_decode_steps_back_to_back_across_a_page_boundary():
+    # rope/append into a page and decode on the cluster plan, eight steps issued
+    # back to back with no host synchronisation; the appended positions cross
+    # from one page into the next.  Each step must see its own and every earlier
+    # appended row.
+    H, D, ps, maxp, steps, start = 32, 128, 128, 32, 8, 1020
+    q0, kp, vp, table = make_single(31, H, D, ps, maxp)
+    assert dattn.dattn_decode_paged_plan(1, H, D, ps, maxp, kp.shape[0])["cluster_size"] > 0
+    g = torch.Generator(device="cuda").manual_seed(32)
+    kp_host, vp_host = to_np(kp).copy(), to_np(vp).copy()
+    tab = torch.from_numpy(table).cuda()
+    toks = [tuple(rand_f16(g, (1, H, D)) for _ in range(3)) for _ in range(steps)]
+    cpts = [cur_pos_tensor([start + t]) for t in range(steps)]
+    q_rots = [torch.empty((1, H, D), dtype=torch.float16, device="cuda") for _ in range(steps)]
+    outs = [torch.empty((1, H, D), dtype=torch.float16, device="cuda") for _ in range(steps)]
+    n = _native.dattn_decode_workspace_bytes(1, H, D, ps * maxp, 0)
+    ws = torch.empty((max(n, 16),), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    for t in range(steps):
+        q, kn, vn = toks[t]
+        dattn.rope_append(q, kn, vn, kp, vp, cpts[t], block_table=tab, q_out=q_rots[t])
+        dattn.decode_paged(q_rots[t], kp, vp, tab, cpts[t], out=outs[t], workspace=ws)
+    torch.cuda.synchronize()
+    for t in range(steps):
+        q, kn, vn = toks[t]
+        cp = [start + t]
+        page, row = int(table[0, cp[0] // ps]), cp[0] % ps
+        kp_host[page, row] = oracle.rope_f64(to_np(kn), cp).astype(np.float16)[0]
+        vp_host[page, row] = to_np(vn)[0]
+        q_ref = oracle.rope_f64(to_np(q), cp).astype(np.float16)
+        ref = oracle.decode_paged_f64(q_ref, kp_host, vp_host, table, np.asarray(cp, np.uint32))
+        assert_decode_close(outs[t], ref, f"step {t} (position {cp[0]})")
+
+
+def test_recorded_batch_replays_on_new_pages_and_table():
+    # a recorded submission keeps the pool's address (in the tensor maps) and
+    # reads the block table, current_pos and the pages at replay
+    H, D, ps, maxp = 32, 128, 128, 16
+    q, kp, vp, table = make_single(41, H, D, ps, maxp, extra=8)
+    assert dattn.dattn_decode_paged_plan(1, H, D, ps, maxp, kp.shape[0])["cluster_size"] > 0
+    g = torch.Generator(device="cuda").manual_seed(42)
+    tab = torch.from_numpy(table).cuda()
+    cpt = cur_pos_tensor([2000])
+    out = torch.empty_like(q)
+    n = _native.dattn_decode_workspace_bytes(1, H, D, ps * maxp, 0)
+    ws = torch.empty((max(n, 16),), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        dattn.dattn_decode_paged_f16(q, kp, vp, out, tab, cpt, ws, 0, stream=stream)
+        torch.cuda.synchronize()
+        dattn.dattn_batch_begin(stream)
+        dattn.dattn_decode_paged_f16(q, kp, vp, out, tab, cpt, ws, 0, stream=stream)
+        batch = dattn.dattn_batch_end(stream)
+    rng = np.random.default_rng(43)
+    for cp in (2000, 127, 128, 1500):
+        q.normal_(generator=g)
+        kp.normal_(generator=g)
+        vp.normal_(generator=g)
+        table = rng.permutation(kp.shape[0])[:maxp].reshape(1, maxp).astype(np.int32)
+        tab.copy_(torch.from_numpy(table))
+        cpt.fill_(cp)
+        torch.cuda.synchronize()
+        batch.launch(stream)
+        stream.synchronize()
+        ref = oracle.decode_paged_f64(to_np(q), to_np(kp), to_np(vp), table,
+                                      np.asarray([cp], np.uint32))
+        assert_decode_close(out, ref, f"replay cp={cp}")
+    batch.close()
