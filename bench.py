@@ -275,7 +275,7 @@ class Replica:
     """Input sets, outputs and workspace of one workload on one GPU."""
 
     def __init__(self, name: str, device, l2_bytes: int, partitions: int = 0,
-                 batch: int = 0, page_size: int = 0):
+                 batch: int = 0, page_size: int = 0, current_pos: int | None = None):
         import dataclasses
 
         import token_decode_attention_gb300 as dattn
@@ -285,10 +285,14 @@ class Replica:
             # same per-sequence recipe, fewer sequences (small ncu captures)
             self.w = w = dataclasses.replace(w, batch=batch,
                                              description=w.description + f", batch {batch}")
+        if current_pos is not None:
+            # same recipe, another live length (every sequence)
+            self.w = w = dataclasses.replace(w, current_pos=current_pos,
+                                             description=w.description + f", current_pos {current_pos}")
         self.device = device
         kv = w.kv_bytes()
         self.sets_n = input_sets(kv, l2_bytes)
-        base = make_inputs(WORKLOADS[name], device, batch=w.batch)
+        base = make_inputs(w, device, batch=w.batch)
         self.cp_host = base["cur_pos_host"]
         self.page_size = page_size
         if page_size:
@@ -682,13 +686,15 @@ def cpu_sweep(budget_s: float) -> dict:
 
 def sweep(device, stream, l2_bytes: int, steps: int, warmup: int, peak: float) -> dict:
     res = {}
-    runs = [(n, 0) for n in ("small", "7b", "ragged", "long", "outlier")]
-    runs += [(n, 16) for n in ("7b", "ragged", "long", "outlier")]
-    runs += [("7b", 128)]  # pages large enough for the cluster plan
-    for name, ps in runs:
-        key = name if not ps else f"{name}_paged{ps}"
+    runs = [(n, 0, None) for n in ("small", "7b", "ragged", "long", "outlier")]
+    # a live length whose CTA ranges end inside a stage (most lengths do)
+    runs += [("7b", 0, 3332)]
+    runs += [(n, 16, None) for n in ("7b", "ragged", "long", "outlier")]
+    runs += [("7b", 128, None)]  # pages large enough for the cluster plan
+    for name, ps, cp in runs:
+        key = name + (f"_paged{ps}" if ps else "") + (f"_cp{cp}" if cp is not None else "")
         try:
-            r = Replica(name, device, l2_bytes, page_size=ps)
+            r = Replica(name, device, l2_bytes, page_size=ps, current_pos=cp)
             ms, _ = r.timed(steps, warmup, stream, 1, soak_s=0.2)
             pct = r.step_percentiles(max(20, steps), stream)
             t = ms * 1e-3 / steps

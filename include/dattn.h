@@ -163,12 +163,16 @@ int dattn_decode_workspace_bytes(int batch, int n_heads, int head_dim, int seq_l
  * For each sequence b and head h, with L = min(current_pos[b], seq_len-1) + 1:
  *   out[b,h,:] = sum_{p<L} softmax_p(Q[b,h,:].K[b,p,h,:] / sqrt(head_dim)) V[b,p,h,:]
  * computed with fp32 accumulation and an online (running max/sum) softmax, then
- * rounded to f16 (round to nearest even).  Positions p >= L are never read: the
- * page's -infinity score gives them weight exactly zero.  The live positions are
- * divided among CTAs (see dattn_plan); the partial softmax states of a
- * sequence that spans several CTAs are merged (log-sum-exp merge) by a second
- * kernel, or, in the cluster plan, through distributed shared memory within
- * the same launch.  Everything is enqueued on `stream`.
+ * rounded to f16 (round to nearest even).  Positions p >= L never enter the
+ * computation, whatever their contents (NaN included): the page's -infinity
+ * score gives them weight exactly zero.  (Their memory may still be touched:
+ * the L2 prefetch described under dattn_decode_paged_f16 works on ranges
+ * planned for full caches, and a paged cache's last live page is copied
+ * whole.)  The live positions are divided among CTAs (see dattn_plan); the
+ * partial softmax states of a sequence that spans several CTAs are merged
+ * (log-sum-exp merge) by a second kernel, or, in the cluster plan, through
+ * distributed shared memory within the same launch.  Everything is enqueued on
+ * `stream`.
  *
  * Concurrent calls on different streams need different workspaces.
  * A return of DATTN_OK means the kernels were enqueued.  The output is valid

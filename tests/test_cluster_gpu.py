@@ -84,8 +84,12 @@ def test_single_sequence(H, D, S, cp):
     assert_decode_close(out, ref, f"H={H} D={D} S={S} cp={cp} plan={plan}")
 
 
-def test_positions_past_current_pos_are_never_read():
-    H, D, S, cp = 32, 128, 4096, 2500
+@pytest.mark.parametrize("cp", [2500, 4000, 130, 5])
+def test_positions_past_current_pos_are_never_read(cp):
+    # live lengths whose CTA ranges end inside a stage: each range's last stage
+    # is copied as a whole tensor box ending where the range ends (its first
+    # rows are rows before the range, or the fill value below position 0)
+    H, D, S = 32, 128, 4096
     g = torch.Generator(device="cuda").manual_seed(77)
     q, k, v = rand_f16(g, (1, H, D)), rand_f16(g, (1, S, H, D)), rand_f16(g, (1, S, H, D))
     cpt = cur_pos_tensor([cp])
@@ -97,6 +101,8 @@ def test_positions_past_current_pos_are_never_read():
     torch.cuda.synchronize()
     assert dattn.dattn_decode_plan(1, H, D, S)["cluster_size"] > 0
     assert torch.equal(clean, poisoned)
+    ref = oracle.decode_f64(to_np(q), to_np(k), to_np(v), np.asarray([cp], np.uint32))
+    assert_decode_close(clean, ref, f"cp={cp}")
 
 
 def test_against_split_plan_and_oracle_outlier_channels():

@@ -281,3 +281,24 @@ def test_recorded_batch_replays_on_new_pages_and_table():
                                       np.asarray([cp], np.uint32))
         assert_decode_close(out, ref, f"replay cp={cp}")
     batch.close()
+
+
+def test_rows_past_current_pos_in_the_last_page_have_no_effect():
+    # the unit's last, partial page is copied whole (one tensor box); its rows
+    # past current_pos land in shared memory but are never read
+    H, D, ps, maxp = 32, 128, 128, 16
+    q, kp, vp, table = make_single(51, H, D, ps, maxp)
+    assert dattn.dattn_decode_paged_plan(1, H, D, ps, maxp, kp.shape[0])["cluster_size"] > 0
+    tab = torch.from_numpy(table).cuda()
+    for cp in (1000, 1023, 1024, 5):
+        base = dattn.decode_paged(q, kp, vp, tab, cur_pos_tensor([cp])).clone()
+        kp2, vp2 = kp.clone(), vp.clone()
+        last = int(table[0, cp // ps])
+        kp2[last, cp % ps + 1:] = float("nan")
+        vp2[last, cp % ps + 1:] = float("inf")
+        out = dattn.decode_paged(q, kp2, vp2, tab, cur_pos_tensor([cp]))
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), base.view(torch.int16)), cp
+        ref = oracle.decode_paged_f64(to_np(q), to_np(kp), to_np(vp), table,
+                                      np.asarray([cp], np.uint32))
+        assert_decode_close(out, ref, f"cp={cp}")

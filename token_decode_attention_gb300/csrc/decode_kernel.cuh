@@ -216,10 +216,12 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     // Before waiting, thread 0 prefetches into L2 the first positions of the
     // range this CTA would own if every sequence were full (the range depends on
     // current_pos, which may not be final yet).  Kernel parameters alone give
-    // that range, so nothing the previous kernel writes is read; a prefetch only
-    // warms L2, the point of coherence, so the reads after the wait still see
-    // the final data.  Exact when the caches are full; elsewhere some of it is
-    // read by other CTAs, the rest is wasted bandwidth.
+    // that range; a prefetch only warms L2, the point of coherence, so the
+    // reads after the wait still see the final data.  Exact when the caches are
+    // full; elsewhere some of it is read by other CTAs, the rest is wasted
+    // bandwidth.  The cluster plan (one sequence) takes the range from
+    // current_pos read before the wait instead, as a hint: exact unless the
+    // kernel before this one changes current_pos.
     //
     // A paged cache finds its pages through the block table, which the previous
     // kernel may still be writing: the entries read here are only used to pick
@@ -230,13 +232,22 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         // capacity (every sequence full): the host keeps c * Wc in 64 bits
         const long long Wc = static_cast<long long>(a.B) * nhg * S;
         long long x, x_lim;
-        if constexpr (CLUSTER) {  // CTA r of cluster u: [r S / C, (r+1) S / C) of unit u
+        if constexpr (CLUSTER) {
+            // CTA r of cluster u: the range it will own if current_pos is
+            // final already, [r L / C, (r+1) L / C) of unit u.  current_pos is
+            // read here as a hint only, through L2 (no L1 line is left behind
+            // for the read after the wait).
             const long long u = blockIdx.x / a.cluster;
             const long long r = blockIdx.x - u * a.cluster;
-            long long r0 = r * S / a.cluster;
-            if constexpr (MODE == kModeClusterPaged) r0 -= r0 % a.page_size;  // ranges start on a page
+            const uint32_t cph = __ldcg(a.cur_pos + u / nhg);
+            const long long Lh = cph >= static_cast<uint32_t>(S - 1) ? S : static_cast<long long>(cph) + 1;
+            long long r0 = r * Lh / a.cluster, r1 = (r + 1) * Lh / a.cluster;
+            if constexpr (MODE == kModeClusterPaged) {  // ranges start on a page
+                r0 -= r0 % a.page_size;
+                r1 = r + 1 == a.cluster ? Lh : r1 - r1 % a.page_size;
+            }
             x = u * S + r0;
-            x_lim = u * S + (r + 1) * S / a.cluster;
+            x_lim = u * S + r1;
         } else {
             x = static_cast<long long>(blockIdx.x) * Wc / a.partitions;
             x_lim = static_cast<long long>(blockIdx.x + 1) * Wc / a.partitions;
@@ -529,7 +540,13 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                 const int pos0 = walk.off + p;
                 __half *dK = ring + static_cast<size_t>(slot) * 2 * buf_elems;
                 __half *dV = dK + buf_elems;
-                if (lane == 0) mbar_arrive_expect_tx(&full_bar[slot], 2u * np * row_bytes);
+                // rows the stage's copies write: with tensor boxes a partial
+                // stage still lands whole boxes (a full stage of a dense cache,
+                // whole pages of a paged one)
+                int tx_rows = np;
+                if (tmap_ok && !contiguous)
+                    tx_rows = paged ? (np + a.page_size - 1) / a.page_size * a.page_size : a.stage_pos;
+                if (lane == 0) mbar_arrive_expect_tx(&full_bar[slot], 2u * tx_rows * row_bytes);
                 __syncwarp();
                 if (!paged) {
                     const __half *sK = Kb + static_cast<size_t>(pos0) * pos_stride;
@@ -539,12 +556,17 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                             bulk_g2s(dK, sK, np * row_bytes, &full_bar[slot], policy);
                             bulk_g2s(dV, sV, np * row_bytes, &full_bar[slot], policy);
                         }
-                    } else if (tmap_ok && np == a.box_pos) {
-                        // a full stage of the head group: one tensor box each
+                    } else if (tmap_ok) {
+                        // a stage of the head group: one tensor box each
                         // ({D, HG, P} at row b*S + pos0; the host checked that
-                        // B*S fits the 32-bit coordinate)
+                        // B*S fits the 32-bit coordinate).  A partial stage
+                        // (the range's last) takes the box that ends where the
+                        // range ends: its first P - np rows are rows this CTA
+                        // read just before (L2 hits), or the fill value where
+                        // the coordinate is negative, and the consumers start
+                        // at row P - np.
                         if (lane == 0) {
-                            const int row0 = static_cast<int>(walk.b * a.S + pos0);
+                            const int row0 = static_cast<int>(walk.b * a.S + pos0 + np - a.stage_pos);
                             tensor3d_g2s(dK, &a.tmap_k, 0, h0, row0, &full_bar[slot], policy);
                             tensor3d_g2s(dV, &a.tmap_v, 0, h0, row0, &full_bar[slot], policy);
                         }
@@ -585,9 +607,13 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                                 bulk_g2s(tK, sK, run * row_bytes, &full_bar[slot], policy);
                                 bulk_g2s(tV, sV, run * row_bytes, &full_bar[slot], policy);
                             }
-                        } else if (tmap_ok && run == a.box_pos) {
-                            // a whole page of the head group: one tensor box each
-                            // ({D, HG, page_size} at row page * page_size of the pool)
+                        } else if (tmap_ok) {
+                            // a page of the head group: one tensor box each
+                            // ({D, HG, page_size} at row page * page_size of the
+                            // pool).  Stages start on a page, so every run is a
+                            // page's first `run` rows; the box of the unit's last,
+                            // partial page also lands the page's rows past the
+                            // live length, which the consumers never read.
                             if (lane == 0) {
                                 const int row0 = static_cast<int>(page * a.page_size);
                                 tensor3d_g2s(tK, &a.tmap_k, 0, h0, row0, &full_bar[slot], policy);
@@ -638,6 +664,9 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     const uint32_t consumer_threads = static_cast<uint32_t>(a.active_warps) * 32;
     float *mbuf = reinterpret_cast<float *>(smem + a.merge_offset);
     const int rec = D + 2;
+    // the producer copies a dense cache's head-group stages as tensor boxes
+    // (partial ones ending at the buffer's last row) under this condition
+    const bool tail_box_cta = MODE == kModeCluster && a.use_tmap && (smem_addr(smem) & 127u) == 0;
     int st = 0;
     // ok turns false (for the whole warp) once a pipeline wait has run out.  The
     // warp then skips waits, compute and writes, but keeps walking the pieces
@@ -688,7 +717,11 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
             }
             if (!ok) continue;
             const int np = min(a.stage_pos, walk.len - p);
-            const __half *sK = ring + static_cast<size_t>(slot) * 2 * buf_elems;
+            // a partial stage of a dense cache copied as a tensor box ends at the
+            // buffer's last row (see the producer)
+            const int row_skip = tail_box_cta && hg < a.H && np < a.stage_pos ? a.stage_pos - np : 0;
+            const __half *sK = ring + static_cast<size_t>(slot) * 2 * buf_elems +
+                               static_cast<size_t>(row_skip) * hg * D;
             const __half *sV = sK + buf_elems;
             // One group: NPOS positions of each (head, phase) slot, whose dot
             // products, shuffles and exponentials are independent, so their
