@@ -45,6 +45,10 @@ def test_plan_choice():
     assert dattn.dattn_decode_plan(w.batch, w.n_heads, w.head_dim, w.seq_len)["cluster_size"] == 0
     assert dattn.dattn_decode_plan(64, 32, 128, 2048)["cluster_size"] == 0
     assert dattn.dattn_decode_plan(1, 32, 128, 4096, 37)["cluster_size"] == 0
+    # few heads leave too few CTAs for a cluster plan past the latency-bound sizes
+    for H, S in ((1, 131072), (2, 131072), (4, 65536), (1, 16384)):
+        assert dattn.dattn_decode_plan(1, H, 128, S)["cluster_size"] == 0, (H, S)
+    assert dattn.dattn_decode_plan(1, 1, 128, 256)["cluster_size"] > 0
 
 
 # (n_heads, head_dim, seq_len, current_pos): a single sequence; head counts with

@@ -86,6 +86,25 @@ constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
 // 16-position pages) 21.7 us, against 15.3-15.5 us for the split plan.
 #define DATTN_CLUSTER_PAGED_MIN_COPY_BYTES (32 * 1024)
 #endif
+// The cluster plan streams with fewer CTAs than the split plan (whole clusters
+// must be resident at once), and saves the merge kernel's ~1-2 us.  It is kept
+// only where that trade wins on GB300: at most DATTN_CLUSTER_MAX_CTA_BYTES of
+// K+V capacity per CTA, and at least DATTN_CLUSTER_MIN_CTA_FRACTION of the SMs
+// busy unless the call is latency-bound (at most DATTN_CLUSTER_TINY_CTA_BYTES
+// per CTA).  Measured B=1 (cluster vs split plan): 1 head, 16 CTAs, 100001
+// live positions 48.0 vs 14.2 us; 2 heads, 32 CTAs 48.8 vs 21.1 us; 4 heads,
+// 64 CTAs (2 MiB per CTA) 28.1 vs 21.5 us; 32 heads, 128 CTAs, 16384 positions
+// (2 MiB per CTA) 33.7 vs 32.1 us at 12001 live positions, 40.4 vs 41.8 at
+// 16384; and faster on the cluster plan from 96 CTAs at 1.4 MiB per CTA down.
+#ifndef DATTN_CLUSTER_MAX_CTA_BYTES
+#define DATTN_CLUSTER_MAX_CTA_BYTES (2LL << 20)
+#endif
+#ifndef DATTN_CLUSTER_MIN_CTA_FRACTION
+#define DATTN_CLUSTER_MIN_CTA_FRACTION 0.6
+#endif
+#ifndef DATTN_CLUSTER_TINY_CTA_BYTES
+#define DATTN_CLUSTER_TINY_CTA_BYTES (128LL << 10)
+#endif
 #ifndef DATTN_CLUSTER_MAX_SIZE
 #define DATTN_CLUSTER_MAX_SIZE 16  // CTAs per cluster (8 is the portable limit)
 #endif
@@ -493,6 +512,13 @@ int make_cluster_plan(int B, int H, int D, int S, int page_size, const DeviceInf
             best = q;
             best_ctas = ctas;
         }
+    }
+    if (best.cluster > 0) {
+        const double cta_bytes = cap_bytes / static_cast<double>(best.G);
+        const bool busy = best.G >= DATTN_CLUSTER_MIN_CTA_FRACTION * di.sms;
+        if (cta_bytes > static_cast<double>(DATTN_CLUSTER_MAX_CTA_BYTES) ||
+            (!busy && cta_bytes > static_cast<double>(DATTN_CLUSTER_TINY_CTA_BYTES)))
+            best = Plan();  // the split plan streams faster
     }
     *out = best;
     return DATTN_OK;
