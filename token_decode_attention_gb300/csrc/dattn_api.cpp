@@ -419,7 +419,9 @@ int make_cluster_plan(int B, int H, int D, int S, int page_size, const DeviceInf
     if (cap_bytes > static_cast<double>(DATTN_CLUSTER_MAX_CAPACITY_BYTES)) return DATTN_OK;
     // 32-bit box coordinate (a paged caller checks the rows of its pool)
     if (page_size == 0 && static_cast<double>(B) * S >= 2147483647.0) return DATTN_OK;
-    if (page_size < 0) return DATTN_OK;
+    // a paged cache: a stage is a whole number of pages and a page one tensor
+    // box, whose height is at most 256 rows
+    if (page_size < 0 || page_size > 256) return DATTN_OK;
     const int c8 = D / 8;
     int bdx, ch;
     if (c8 <= 8) {

@@ -22,15 +22,18 @@
 // "pieces" (a run of positions of one unit); a CTA writes the f16 output of a
 // unit it covers whole and the partial softmax state (m, l, acc) of the others
 // for combine.cu.  Positions past L_b belong to no range: the page's -infinity
-// mask is a loop bound and masked rows are never read.
+// mask is a loop bound and masked rows never enter the computation.
 //
-// Cluster plan (the CLUSTER instances; a dense cache of one sequence): the grid
-// is B * NHG thread-block clusters of C CTAs.  Cluster u takes unit u whole and
-// CTA r of it the positions [r L_b / C, (r+1) L_b / C); a head group smaller
-// than H is copied per full stage as one 3D tensor box {D, HG, P}.  Each CTA
-// leaves its partial state in a shared-memory record, and the cluster's CTAs
-// merge the C records through distributed shared memory, each finishing an
-// equal share of the unit's outputs: no workspace and no second kernel.
+// Cluster plan (the cluster instances; one sequence, dense or paged cache):
+// the grid is B * NHG thread-block clusters of C CTAs.  Cluster u takes unit u
+// whole and CTA r of it the positions [r L_b / C, (r+1) L_b / C) (cut at page
+// boundaries for a paged cache); a head group smaller than H is copied as 3D
+// tensor boxes {D, HG, P} per stage (a dense cache; a partial stage takes the
+// box that ends where the range ends) or {D, HG, page_size} per page (a paged
+// cache).  Each CTA leaves its partial state in a shared-memory record, and
+// the cluster's CTAs merge the C records through distributed shared memory,
+// each finishing an equal share of the unit's outputs: no workspace and no
+// second kernel.
 //
 // Per CTA:
 //   * launched with programmatic dependent launch, it initialises its barriers
