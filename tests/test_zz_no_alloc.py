@@ -89,6 +89,26 @@ def test_calls_in_a_row_match_the_workspace_entry_point_bit_for_bit(lib):
     assert _native.dattn_device_error(clear=True) == 0
 
 
+def test_single_sequence_on_the_cluster_plan_matches_bit_for_bit(lib):
+    # one sequence takes the cluster plan, which needs no scratch at all: the
+    # call must still match the workspace entry point exactly, twice in a row
+    g = torch.Generator(device="cuda").manual_seed(20260124)
+    B, H, D, S = 1, 32, 128, 4096
+    plan = _native.dattn_decode_plan(B, H, D, S, 0)
+    assert plan["cluster_size"] > 0 and plan["workspace_bytes"] == 0
+    for i, cp in enumerate(([3000], [4095])):
+        q, k, v = _inputs(g, B, H, D, S)
+        cpt = cur_pos_tensor(cp)
+        out = torch.full((B, H, D), float("nan"), dtype=torch.float16, device="cuda")
+        assert _noalloc(lib, q, k, v, out, cpt) == 0, lib.dattn_last_error().decode()
+        ref = _reference(q, k, v, cpt)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), f"call {i + 1}: differs from dattn_decode_f16_ex"
+    exact = oracle.decode_f64(to_np(q), to_np(k), to_np(v), np.asarray(cp, np.uint32))
+    assert_decode_close(out, exact, "cluster plan against the oracle")
+    assert _native.dattn_device_error(clear=True) == 0
+
+
 def test_shape_beyond_static_scratch_is_rejected(lib):
     # 4096 short sequences x 64 heads need ~140 MB of partial states; the call
     # must fail on the host before launching anything
