@@ -245,9 +245,10 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
             const uint32_t cph = __ldcg(a.cur_pos + u / nhg);
             const long long Lh = cph >= static_cast<uint32_t>(S - 1) ? S : static_cast<long long>(cph) + 1;
             long long r0 = r * Lh / a.cluster, r1 = (r + 1) * Lh / a.cluster;
-            if constexpr (MODE == kModeClusterPaged) {  // ranges start on a page
-                r0 -= r0 % a.page_size;
-                r1 = r + 1 == a.cluster ? Lh : r1 - r1 % a.page_size;
+            if constexpr (MODE == kModeClusterPaged) {  // whole pages, as below
+                const long long pages = (Lh + a.page_size - 1) / a.page_size;
+                r0 = r * pages / a.cluster * a.page_size;
+                r1 = r + 1 == a.cluster ? Lh : (r + 1) * pages / a.cluster * a.page_size;
             }
             x = u * S + r0;
             x_lim = u * S + r1;
@@ -329,10 +330,12 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         const long long g = u - b0 * nhg;
         long long r0 = r * L0 / a.cluster, r1 = (r + 1) * L0 / a.cluster;
         if constexpr (MODE == kModeClusterPaged) {
-            // ranges start on a page, so every stage is whole pages (one tensor
-            // box each) but for the unit's last page
-            r0 -= r0 % a.page_size;
-            r1 = r + 1 == a.cluster ? L0 : r1 - r1 % a.page_size;
+            // the unit's pages dealt out evenly (a CTA takes the floor or the
+            // ceiling of pages / C), so every range starts on a page, and every
+            // stage is whole pages (one tensor box each) but for the unit's last
+            const long long pages = (L0 + a.page_size - 1) / a.page_size;
+            r0 = r * pages / a.cluster * a.page_size;
+            r1 = r + 1 == a.cluster ? L0 : (r + 1) * pages / a.cluster * a.page_size;
         }
         x0 = g * L0 + r0;
         x1 = g * L0 + r1;
