@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     // on the stream finishes.  Everything after the wait sees that kernel's writes
     // (current_pos, Q, the cache).
     //
-    // Before waiting, thread 0 prefetches into L2 the first positions of the
+    // Before waiting, the CTA prefetches into L2 the first positions of the
     // range this CTA would own if every sequence were full (the range depends on
     // current_pos, which may not be final yet).  Kernel parameters alone give
     // that range; a prefetch only warms L2, the point of coherence, so the
@@ -230,7 +230,14 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     // kernel may still be writing: the entries read here are only used to pick
     // what to prefetch, each checked to lie inside the page pool, and are read
     // again after the wait for the copies.  A stale entry wastes a prefetch.
-    if (threadIdx.x == 0 && a.prefetch_positions > 0) {
+    //
+    // Thread 0 issues a dense cache's prefetches.  For a paged cache warp 0
+    // does, one lane per page, so that the block-table reads go out together:
+    // one thread reading the entries one after another (a dependent load per
+    // page) kept warp 0, and with it the CTA's consumers, ~17 us late on a
+    // window of 24 pages.
+    const bool paged_pf = PAGED_OK && a.block_table != nullptr;
+    if (a.prefetch_positions > 0 && (paged_pf ? warp == 0 : threadIdx.x == 0)) {
         const long long S = a.S, nhg = a.head_groups;
         // capacity (every sequence full): the host keeps c * Wc in 64 bits
         const long long Wc = static_cast<long long>(a.B) * nhg * S;
@@ -258,45 +265,51 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
         }
         const long long x_end = min(x + a.prefetch_positions, x_lim);
         const size_t row = static_cast<size_t>(a.H) * a.D;  // halves per position
+        // n positions of heads [h0, h0 + hg) from row first_pos of the cache (or pool)
+        auto prefetch_run = [&](long long first_pos, long long n, int h0, int hg) {
+            const __half *k0 = reinterpret_cast<const __half *>(a.K) + static_cast<size_t>(first_pos) * row;
+            const __half *v0 = reinterpret_cast<const __half *>(a.V) + static_cast<size_t>(first_pos) * row;
+            if (hg == a.H) {  // all heads: the run is one span
+                const uint32_t bytes = static_cast<uint32_t>(n * row * 2);
+                bulk_prefetch_l2(k0, bytes);
+                bulk_prefetch_l2(v0, bytes);
+            } else if (CLUSTER && a.use_tmap) {  // a head group: whole tensor boxes
+                for (long long j = 0; j + a.box_pos <= n; j += a.box_pos) {
+                    const int row0 = static_cast<int>(first_pos + j);
+                    tensor3d_prefetch_l2(&a.tmap_k, 0, h0, row0);
+                    tensor3d_prefetch_l2(&a.tmap_v, 0, h0, row0);
+                }
+            } else {  // a head group: one span per position
+                const uint32_t bytes = static_cast<uint32_t>(hg) * a.D * 2;
+                for (long long j = 0; j < n; ++j) {
+                    const size_t o = static_cast<size_t>(j) * row + static_cast<size_t>(h0) * a.D;
+                    bulk_prefetch_l2(k0 + o, bytes);
+                    bulk_prefetch_l2(v0 + o, bytes);
+                }
+            }
+        };
         while (x < x_end) {
             const long long u = x / S;  // unit (b, g)
             const long long off = x - u * S;
             const long long b = u / nhg;
             const int h0 = static_cast<int>(u - b * nhg) * a.heads_per_cta;
             const int hg = min(a.heads_per_cta, a.H - h0);
-            long long n = min(S - off, x_end - x);
-            long long first_pos = b * S + off;  // dense: row index in [B*S]
-            bool go = true;
-            if (PAGED_OK && a.block_table != nullptr) {
-                const long long pidx = off / a.page_size;
-                const long long in_page = off - pidx * a.page_size;
-                n = min(n, static_cast<long long>(a.page_size) - in_page);
-                // through L2 only (no L1 line is left behind for the reads after the wait)
-                const long long page = __ldcg(a.block_table + b * a.max_pages + pidx);
-                go = page >= 0 && page < a.num_pages;
-                first_pos = page * a.page_size + in_page;
-            }
-            if (go) {
-                const __half *k0 = reinterpret_cast<const __half *>(a.K) + static_cast<size_t>(first_pos) * row;
-                const __half *v0 = reinterpret_cast<const __half *>(a.V) + static_cast<size_t>(first_pos) * row;
-                if (hg == a.H) {  // all heads: the run is one span
-                    const uint32_t bytes = static_cast<uint32_t>(n * row * 2);
-                    bulk_prefetch_l2(k0, bytes);
-                    bulk_prefetch_l2(v0, bytes);
-                } else if (CLUSTER && a.use_tmap) {  // a head group: whole tensor boxes
-                    for (long long j = 0; j + a.box_pos <= n; j += a.box_pos) {
-                        const int row0 = static_cast<int>(first_pos + j);
-                        tensor3d_prefetch_l2(&a.tmap_k, 0, h0, row0);
-                        tensor3d_prefetch_l2(&a.tmap_v, 0, h0, row0);
-                    }
-                } else {  // a head group: one span per position
-                    const uint32_t bytes = static_cast<uint32_t>(hg) * a.D * 2;
-                    for (long long j = 0; j < n; ++j) {
-                        const size_t o = static_cast<size_t>(j) * row + static_cast<size_t>(h0) * a.D;
-                        bulk_prefetch_l2(k0 + o, bytes);
-                        bulk_prefetch_l2(v0 + o, bytes);
+            const long long n = min(S - off, x_end - x);
+            if (paged_pf) {
+                // the unit's pages overlapping [off, off + n): lane l takes
+                // pages p_first + l, + 32, ... (x and n are the same in every lane)
+                const long long ps = a.page_size;
+                const long long p_first = off / ps, p_end = (off + n - 1) / ps + 1;
+                for (long long pidx = p_first + lane; pidx < p_end; pidx += 32) {
+                    // through L2 only (no L1 line is left behind for the reads after the wait)
+                    const long long page = __ldcg(a.block_table + b * a.max_pages + pidx);
+                    if (page >= 0 && page < a.num_pages) {
+                        const long long lo = max(off, pidx * ps), hi = min(off + n, (pidx + 1) * ps);
+                        prefetch_run(page * ps + (lo - pidx * ps), hi - lo, h0, hg);
                     }
                 }
+            } else {
+                prefetch_run(b * S + off, n, h0, hg);  // dense: row index in [B*S]
             }
             x += n;
         }
@@ -584,8 +597,53 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                                      row_bytes, &full_bar[slot], policy);
                         }
                     }
+                } else if (contiguous || tmap_ok) {
+                    // one copy per page and tensor: lane l takes page pa + l
+                    // (+ 32, ...) of the stage's pages pa..pb, so the pages'
+                    // address arithmetic and copies go out side by side
+                    const int pa = pos0 / a.page_size, pb = (pos0 + np - 1) / a.page_size;
+                    for (int q0 = pa; q0 <= pb; q0 += 32) {
+                        if (page_first < 0 || q0 < page_first || min(q0 + 31, pb) >= page_first + 32) {
+                            page_first = q0;
+                            // coherent load: the table may have been written by the
+                            // kernel before this one, after the pre-wait prefetch read it
+                            page_lane = (q0 + lane < a.max_pages) ? __ldcg(bt + q0 + lane) : 0;
+                        }
+                        const int qi = q0 + lane;
+                        long long page = __shfl_sync(kFull, page_lane, (qi - page_first) & 31);
+                        if (qi <= pb) {
+                            if (page < 0 || page >= a.num_pages) {  // never read outside the pages
+                                atomicOr(a.err, kErrPageIndex);
+                                page = 0;
+                            }
+                            const int lo = max(pos0, qi * a.page_size);
+                            const int hi = min(pos0 + np, (qi + 1) * a.page_size);
+                            const int off = lo - qi * a.page_size;
+                            __half *tK = dK + static_cast<size_t>(lo - pos0) * hg * D;
+                            __half *tV = dV + static_cast<size_t>(lo - pos0) * hg * D;
+                            if (contiguous) {
+                                const size_t src = (static_cast<size_t>(page) * a.page_size + off) * pos_stride +
+                                                   static_cast<size_t>(h0) * D;
+                                const uint32_t bytes = static_cast<uint32_t>(hi - lo) * row_bytes;
+                                bulk_g2s(tK, reinterpret_cast<const __half *>(a.K) + src, bytes, &full_bar[slot], policy);
+                                bulk_g2s(tV, reinterpret_cast<const __half *>(a.V) + src, bytes, &full_bar[slot], policy);
+                            } else {
+                                // a page of the head group: one tensor box each
+                                // ({D, HG, page_size} at row page * page_size of
+                                // the pool).  Stages start on a page, so every run
+                                // is a page's first rows; the box of the unit's
+                                // last, partial page also lands the page's rows
+                                // past the live length, which the consumers never
+                                // read.
+                                const int row0 = static_cast<int>(page * a.page_size);
+                                tensor3d_g2s(tK, &a.tmap_k, 0, h0, row0, &full_bar[slot], policy);
+                                tensor3d_g2s(tV, &a.tmap_v, 0, h0, row0, &full_bar[slot], policy);
+                            }
+                        }
+                    }
                 } else {
-                    // split the stage into runs that stay inside one page
+                    // a head group of a paged cache without tensor boxes: runs
+                    // that stay inside one page, one copy per position
                     for (int j = 0; j < np;) {
                         const int pos = pos0 + j;
                         const int pidx = pos / a.page_size;
@@ -608,30 +666,11 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                         const __half *sV = reinterpret_cast<const __half *>(a.V) + src;
                         __half *tK = dK + static_cast<size_t>(j) * hg * D;
                         __half *tV = dV + static_cast<size_t>(j) * hg * D;
-                        if (contiguous) {
-                            if (lane == 0) {
-                                bulk_g2s(tK, sK, run * row_bytes, &full_bar[slot], policy);
-                                bulk_g2s(tV, sV, run * row_bytes, &full_bar[slot], policy);
-                            }
-                        } else if (tmap_ok) {
-                            // a page of the head group: one tensor box each
-                            // ({D, HG, page_size} at row page * page_size of the
-                            // pool).  Stages start on a page, so every run is a
-                            // page's first `run` rows; the box of the unit's last,
-                            // partial page also lands the page's rows past the
-                            // live length, which the consumers never read.
-                            if (lane == 0) {
-                                const int row0 = static_cast<int>(page * a.page_size);
-                                tensor3d_g2s(tK, &a.tmap_k, 0, h0, row0, &full_bar[slot], policy);
-                                tensor3d_g2s(tV, &a.tmap_v, 0, h0, row0, &full_bar[slot], policy);
-                            }
-                        } else {
-                            for (int r = lane; r < run; r += 32) {
-                                bulk_g2s(tK + static_cast<size_t>(r) * hg * D, sK + r * pos_stride,
-                                         row_bytes, &full_bar[slot], policy);
-                                bulk_g2s(tV + static_cast<size_t>(r) * hg * D, sV + r * pos_stride,
-                                         row_bytes, &full_bar[slot], policy);
-                            }
+                        for (int r = lane; r < run; r += 32) {
+                            bulk_g2s(tK + static_cast<size_t>(r) * hg * D, sK + r * pos_stride,
+                                     row_bytes, &full_bar[slot], policy);
+                            bulk_g2s(tV + static_cast<size_t>(r) * hg * D, sV + r * pos_stride,
+                                     row_bytes, &full_bar[slot], policy);
                         }
                         j += run;
                     }
