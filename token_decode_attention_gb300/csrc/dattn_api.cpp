@@ -41,14 +41,18 @@ constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
 #ifndef DATTN_STAGE_BYTES_ONE_PER_SM
 #define DATTN_STAGE_BYTES_ONE_PER_SM (64 * 1024)
 #endif
-// Rows of at most DATTN_SMALL_ROW_BYTES per position (few heads) take larger
-// stages at one CTA per SM: two of 96 KB instead of three of 64 KB, the same
-// ring, fewer and larger copies and more positions per stage for the
-// consumers.  Measured (split plan, graph replay): B=64 H=8 D=128 ragged 46.4
-// -> 43.0 us, B=256 H=8 D=64 55.9 -> 53.1 us, B=16 H=8 S=8192 41.7 -> 39.0 us,
-// B=8 H=4 18.5 -> 17.5 us.  For 8 KB rows the same change measured -1.5 %
-// dense and +0.5 % paged, and for the 10 KB rows of 40 heads +0.7 % (only two
-// 80 KB stages fit), so larger rows keep 64 KB stages.
+// At one CTA per SM a dense cache takes two stages of ~100 KB rather than
+// three of 64 KB: about the same ring, fewer and larger copies and more
+// positions per stage for the consumers.  Measured (split plan, graph replay,
+// same runs): long 298-301 -> 294.5 us, ragged 150.1 -> 149.0 us, outlier
+// 5705-5718 -> 5700-5708 us; few heads (rows of at most 4 KB) 5-8 %, e.g.
+// B=64 H=8 ragged 46.5 -> 42.9 us, B=1 H=4 S=65536 21.4 -> 19.8 us.  Stages of
+// 96 KB gave the 10 KB rows of 40 heads only two 80 KB stages: +0.7 %.  A paged
+// cache gains only with small rows (its larger rows measured +0.3 to +0.9 %
+// with ~100 KB stages), so its rows above DATTN_SMALL_ROW_BYTES keep 64 KB.
+#ifndef DATTN_STAGE_BYTES_DENSE
+#define DATTN_STAGE_BYTES_DENSE (100 * 1024)
+#endif
 #ifndef DATTN_SMALL_ROW_BYTES
 #define DATTN_SMALL_ROW_BYTES 4096
 #endif
@@ -274,8 +278,9 @@ int lcm_int(int x, int y) {
     return x / a * y;
 }
 
-// The split (stream-K) plan with at least `min_groups` head groups.
-int split_plan(int B, int H, int D, int S, int num_partitions, int min_groups,
+// The split (stream-K) plan with at least `min_groups` head groups, for a
+// dense or a paged cache.
+int split_plan(int B, int H, int D, int S, int num_partitions, int min_groups, bool paged,
                const DeviceInfo &di, Plan *out) {
     Plan p;
     p.sms = di.sms;
@@ -317,6 +322,7 @@ int split_plan(int B, int H, int D, int S, int num_partitions, int min_groups,
     const bool deep = dattn::decode_min_blocks(nwc) == 1 ||
                       capacity_pos < kDeepRingPositions * 2LL * di.sms;
     const int stage_target = !deep                               ? kStageTargetBytes
+                             : !paged                             ? DATTN_STAGE_BYTES_DENSE
                              : row_bytes <= DATTN_SMALL_ROW_BYTES ? DATTN_STAGE_BYTES_SMALL_ROWS
                                                                   : kStageTargetBytesOnePerSm;
     int P = std::max(1, std::min(256, stage_target / 2 / row_bytes));
@@ -400,7 +406,8 @@ int make_plan(int B, int H, int D, int S, int num_partitions, int page_size, Pla
         }
     }
     Plan p;
-    if (int st = split_plan(B, H, D, S, num_partitions, DATTN_MIN_HEAD_GROUPS, di, &p)) return st;
+    if (int st = split_plan(B, H, D, S, num_partitions, DATTN_MIN_HEAD_GROUPS, page_size != 0, di, &p))
+        return st;
     // Few sequences (dense cache, library-chosen partitions): one cluster of
     // CTAs per (sequence, head group), merged in distributed shared memory,
     // when such a plan exists.
