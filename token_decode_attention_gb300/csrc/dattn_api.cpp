@@ -321,12 +321,22 @@ int split_plan(int B, int H, int D, int S, int num_partitions, int min_groups, b
     const long long capacity_pos = static_cast<long long>(B) * p.NHG * S;
     const bool deep = dattn::decode_min_blocks(nwc) == 1 ||
                       capacity_pos < kDeepRingPositions * 2LL * di.sms;
-    const int stage_target = !deep                               ? kStageTargetBytes
-                             : !paged                             ? DATTN_STAGE_BYTES_DENSE
-                             : row_bytes <= DATTN_SMALL_ROW_BYTES ? DATTN_STAGE_BYTES_SMALL_ROWS
-                                                                  : kStageTargetBytesOnePerSm;
-    int P = std::max(1, std::min(256, stage_target / 2 / row_bytes));
-    P = std::max(p.PHI, P / p.PHI * p.PHI);
+    const long long slots = static_cast<long long>(di.sms) * (deep ? 1 : 2);
+    auto stage_positions = [&](int target) {
+        const int q = std::max(1, std::min(256, target / 2 / row_bytes));
+        return std::max(p.PHI, q / p.PHI * p.PHI);
+    };
+    int P = stage_positions(deep ? kStageTargetBytesOnePerSm : kStageTargetBytes);
+    // the larger stages, where the batch gives every CTA slot two of them (a
+    // smaller batch takes the smaller stages below, as before)
+    const int big_target = !deep                               ? 0
+                           : !paged                             ? DATTN_STAGE_BYTES_DENSE
+                           : row_bytes <= DATTN_SMALL_ROW_BYTES ? DATTN_STAGE_BYTES_SMALL_ROWS
+                                                                : 0;
+    if (big_target > 0) {
+        const int Pb = stage_positions(big_target);
+        if (capacity_pos >= slots * 2LL * Pb) P = Pb;
+    }
     // A batch too small to give every CTA slot two stages takes smaller stages,
     // for more partitions: such a decode is bound by latency, not by the
     // per-stage overhead that large stages amortise.
@@ -334,7 +344,6 @@ int split_plan(int B, int H, int D, int S, int num_partitions, int min_groups, b
 #define DATTN_SMALL_BATCH_STAGES 1
 #endif
     if (DATTN_SMALL_BATCH_STAGES) {
-        const long long slots = static_cast<long long>(di.sms) * (deep ? 1 : 2);
         while (P / 2 >= p.PHI && 2 * P > kMinPositions && capacity_pos < slots * 2LL * P)
             P = std::max(p.PHI, P / 2 / p.PHI * p.PHI);
     }

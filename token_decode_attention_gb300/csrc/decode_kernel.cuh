@@ -597,10 +597,10 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                                      row_bytes, &full_bar[slot], policy);
                         }
                     }
-                } else if (contiguous || tmap_ok) {
-                    // one copy per page and tensor: lane l takes page pa + l
-                    // (+ 32, ...) of the stage's pages pa..pb, so the pages'
-                    // address arithmetic and copies go out side by side
+                } else {
+                    // paged: lane l takes page pa + l (+ 32, ...) of the stage's
+                    // pages pa..pb, so the pages' address arithmetic and copies
+                    // go out side by side
                     const int pa = pos0 / a.page_size, pb = (pos0 + np - 1) / a.page_size;
                     for (int q0 = pa; q0 <= pb; q0 += 32) {
                         if (page_first < 0 || q0 < page_first || min(q0 + 31, pb) >= page_first + 32) {
@@ -617,17 +617,10 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                                 page = 0;
                             }
                             const int lo = max(pos0, qi * a.page_size);
-                            const int hi = min(pos0 + np, (qi + 1) * a.page_size);
-                            const int off = lo - qi * a.page_size;
+                            const int run = min(pos0 + np, (qi + 1) * a.page_size) - lo;
                             __half *tK = dK + static_cast<size_t>(lo - pos0) * hg * D;
                             __half *tV = dV + static_cast<size_t>(lo - pos0) * hg * D;
-                            if (contiguous) {
-                                const size_t src = (static_cast<size_t>(page) * a.page_size + off) * pos_stride +
-                                                   static_cast<size_t>(h0) * D;
-                                const uint32_t bytes = static_cast<uint32_t>(hi - lo) * row_bytes;
-                                bulk_g2s(tK, reinterpret_cast<const __half *>(a.K) + src, bytes, &full_bar[slot], policy);
-                                bulk_g2s(tV, reinterpret_cast<const __half *>(a.V) + src, bytes, &full_bar[slot], policy);
-                            } else {
+                            if (tmap_ok && !contiguous) {
                                 // a page of the head group: one tensor box each
                                 // ({D, HG, page_size} at row page * page_size of
                                 // the pool).  Stages start on a page, so every run
@@ -638,41 +631,24 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
                                 const int row0 = static_cast<int>(page * a.page_size);
                                 tensor3d_g2s(tK, &a.tmap_k, 0, h0, row0, &full_bar[slot], policy);
                                 tensor3d_g2s(tV, &a.tmap_v, 0, h0, row0, &full_bar[slot], policy);
+                            } else {
+                                const size_t src = (static_cast<size_t>(page) * a.page_size + lo - qi * a.page_size) *
+                                                       pos_stride + static_cast<size_t>(h0) * D;
+                                const __half *sK = reinterpret_cast<const __half *>(a.K) + src;
+                                const __half *sV = reinterpret_cast<const __half *>(a.V) + src;
+                                if (contiguous) {  // the run is one span
+                                    bulk_g2s(tK, sK, run * row_bytes, &full_bar[slot], policy);
+                                    bulk_g2s(tV, sV, run * row_bytes, &full_bar[slot], policy);
+                                } else {  // a head group: one copy per position
+                                    for (int r = 0; r < run; ++r) {
+                                        bulk_g2s(tK + static_cast<size_t>(r) * hg * D, sK + r * pos_stride,
+                                                 row_bytes, &full_bar[slot], policy);
+                                        bulk_g2s(tV + static_cast<size_t>(r) * hg * D, sV + r * pos_stride,
+                                                 row_bytes, &full_bar[slot], policy);
+                                    }
+                                }
                             }
                         }
-                    }
-                } else {
-                    // a head group of a paged cache without tensor boxes: runs
-                    // that stay inside one page, one copy per position
-                    for (int j = 0; j < np;) {
-                        const int pos = pos0 + j;
-                        const int pidx = pos / a.page_size;
-                        const int off = pos - pidx * a.page_size;
-                        if (page_first < 0 || pidx < page_first || pidx >= page_first + 32) {
-                            page_first = pidx;
-                            // coherent load: the table may have been written by the
-                            // kernel before this one, after the pre-wait prefetch read it
-                            page_lane = (pidx + lane < a.max_pages) ? __ldcg(bt + pidx + lane) : 0;
-                        }
-                        long long page = __shfl_sync(kFull, page_lane, pidx - page_first);
-                        if (page < 0 || page >= a.num_pages) {  // never read outside the pages
-                            if (lane == 0) atomicOr(a.err, kErrPageIndex);
-                            page = 0;
-                        }
-                        const int run = min(a.page_size - off, np - j);
-                        const size_t src = (static_cast<size_t>(page) * a.page_size + off) * pos_stride +
-                                           static_cast<size_t>(h0) * D;
-                        const __half *sK = reinterpret_cast<const __half *>(a.K) + src;
-                        const __half *sV = reinterpret_cast<const __half *>(a.V) + src;
-                        __half *tK = dK + static_cast<size_t>(j) * hg * D;
-                        __half *tV = dV + static_cast<size_t>(j) * hg * D;
-                        for (int r = lane; r < run; r += 32) {
-                            bulk_g2s(tK + static_cast<size_t>(r) * hg * D, sK + r * pos_stride,
-                                     row_bytes, &full_bar[slot], policy);
-                            bulk_g2s(tV + static_cast<size_t>(r) * hg * D, sV + r * pos_stride,
-                                     row_bytes, &full_bar[slot], policy);
-                        }
-                        j += run;
                     }
                 }
                 ++issued;
