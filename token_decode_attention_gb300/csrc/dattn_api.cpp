@@ -653,6 +653,11 @@ int launch_decode(const Plan &p, const void *Q, const void *K, const void *V, vo
     // dense or paged cache: prefetch the first stages into L2 before the wait on
     // the previous kernel
     a.prefetch_positions = DATTN_PREFETCH_STAGES > 0 ? DATTN_PREFETCH_STAGES * p.P : 0;
+    // a window of a few pages is read by one thread (7b in 16-position pages,
+    // a one-page window: 0.1 us faster than the warp); larger windows by one
+    // lane per page
+    a.prefetch_lanes =
+        pg.table != nullptr && a.prefetch_positions >= 4LL * pg.page_size ? 32 : 1;
     a.cluster = p.cluster;
     a.use_tmap = p.use_tmap;
     a.rec_offset = p.rec_offset;

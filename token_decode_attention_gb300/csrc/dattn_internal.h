@@ -78,6 +78,7 @@ struct DecodeArgs {
     int cluster;
     int use_tmap;      // full stages (pages) of a head group are copied as tensor boxes
     int box_pos;       // positions of a tensor box: a stage (dense) or a page (paged)
+    int prefetch_lanes;  // paged cache: lanes of warp 0 that read the prefetch window's pages (1..32)
     // Cluster mode: byte offset of this CTA's record [HG][D + 2] of its
     // partial state (m, l, acc) per head, read by the cluster's other CTAs.
     int rec_offset;

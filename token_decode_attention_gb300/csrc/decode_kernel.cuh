@@ -231,13 +231,14 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
     // what to prefetch, each checked to lie inside the page pool, and are read
     // again after the wait for the copies.  A stale entry wastes a prefetch.
     //
-    // Thread 0 issues a dense cache's prefetches.  For a paged cache warp 0
-    // does, one lane per page, so that the block-table reads go out together:
-    // one thread reading the entries one after another (a dependent load per
-    // page) kept warp 0, and with it the CTA's consumers, ~17 us late on a
-    // window of 24 pages.
+    // Thread 0 issues a dense cache's prefetches.  For a paged cache whose
+    // window spans several pages the first prefetch_lanes lanes of warp 0 do,
+    // one lane per page, so that the block-table reads go out together: one
+    // thread reading the entries one after another (a dependent load per page)
+    // kept warp 0, and with it the CTA's consumers, ~17 us late on a window of
+    // 24 pages.
     const bool paged_pf = PAGED_OK && a.block_table != nullptr;
-    if (a.prefetch_positions > 0 && (paged_pf ? warp == 0 : threadIdx.x == 0)) {
+    if (a.prefetch_positions > 0 && threadIdx.x < (paged_pf ? a.prefetch_lanes : 1)) {
         const long long S = a.S, nhg = a.head_groups;
         // capacity (every sequence full): the host keeps c * Wc in 64 bits
         const long long Wc = static_cast<long long>(a.B) * nhg * S;
@@ -297,10 +298,11 @@ __global__ void __launch_bounds__(decode_threads(NWC), decode_min_blocks(NWC))
             const long long n = min(S - off, x_end - x);
             if (paged_pf) {
                 // the unit's pages overlapping [off, off + n): lane l takes
-                // pages p_first + l, + 32, ... (x and n are the same in every lane)
+                // pages p_first + l, + prefetch_lanes, ... (x and n are the same
+                // in every lane)
                 const long long ps = a.page_size;
                 const long long p_first = off / ps, p_end = (off + n - 1) / ps + 1;
-                for (long long pidx = p_first + lane; pidx < p_end; pidx += 32) {
+                for (long long pidx = p_first + lane; pidx < p_end; pidx += a.prefetch_lanes) {
                     // through L2 only (no L1 line is left behind for the reads after the wait)
                     const long long page = __ldcg(a.block_table + b * a.max_pages + pidx);
                     if (page >= 0 && page < a.num_pages) {
