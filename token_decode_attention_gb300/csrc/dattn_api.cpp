@@ -53,6 +53,14 @@ constexpr int kMaxRowBytesKV = 48 * 1024; // K+V bytes per position a CTA stages
 #ifndef DATTN_STAGE_BYTES_DENSE
 #define DATTN_STAGE_BYTES_DENSE (100 * 1024)
 #endif
+// Measured (ragged lengths unless noted): with 2, B=4 H=8 D=128 S=2048 took
+// 13.1 us against 12.1 with the smaller stages; with 4 the few-head gains above
+// stay (B=1 H=1 S=131072 13.5 us, B=1 H=4 S=65536 19.8 us); with 8 or 16 they
+// are lost (14.3 / 21.4 us) while B=4 H=8 D=256 (17.6 -> 17.0 us) and B=4 H=32
+// (14.0 -> 13.3 us at 16) would gain.
+#ifndef DATTN_BIG_STAGES_PER_SLOT
+#define DATTN_BIG_STAGES_PER_SLOT 4
+#endif
 #ifndef DATTN_SMALL_ROW_BYTES
 #define DATTN_SMALL_ROW_BYTES 4096
 #endif
@@ -327,15 +335,16 @@ int split_plan(int B, int H, int D, int S, int num_partitions, int min_groups, b
         return std::max(p.PHI, q / p.PHI * p.PHI);
     };
     int P = stage_positions(deep ? kStageTargetBytesOnePerSm : kStageTargetBytes);
-    // the larger stages, where the batch gives every CTA slot two of them (a
-    // smaller batch takes the smaller stages below, as before)
+    // the larger stages, where the batch's capacity gives every CTA slot
+    // DATTN_BIG_STAGES_PER_SLOT of them (a smaller batch is bound by latency
+    // and keeps the smaller stages, more of them in flight)
     const int big_target = !deep                               ? 0
                            : !paged                             ? DATTN_STAGE_BYTES_DENSE
                            : row_bytes <= DATTN_SMALL_ROW_BYTES ? DATTN_STAGE_BYTES_SMALL_ROWS
                                                                 : 0;
     if (big_target > 0) {
         const int Pb = stage_positions(big_target);
-        if (capacity_pos >= slots * 2LL * Pb) P = Pb;
+        if (capacity_pos >= slots * static_cast<long long>(DATTN_BIG_STAGES_PER_SLOT) * Pb) P = Pb;
     }
     // A batch too small to give every CTA slot two stages takes smaller stages,
     // for more partitions: such a decode is bound by latency, not by the
