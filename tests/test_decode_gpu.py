@@ -307,3 +307,30 @@ def test_empty_partitions_are_skipped_whatever_the_workspace_holds(B, H, D, S, c
     torch.cuda.synchronize()
     ref = oracle.decode_f64(to_np(q), to_np(k), to_np(v), np.asarray(cp, np.uint32))
     assert_decode_close(out, ref, f"W={sum(min(c, S - 1) + 1 for c in cp)} G={partitions}")
+
+
+# few heads (rows of at most 4 KB per position): the split plan's larger
+# stages, and the shapes where it keeps the smaller ones; B, H, D, S, current_pos
+# (None: drawn uniformly per sequence)
+FEW_HEAD_SHAPES = [
+    (1, 1, 128, 131072, [100000]),
+    (1, 4, 128, 65536, [50000]),
+    (4, 1, 128, 65536, [65535, 65535, 65535, 65535]),
+    (64, 8, 128, 2048, None),
+    (4, 8, 256, 2048, None),
+    (16, 8, 64, 1024, None),
+]
+
+
+@pytest.mark.parametrize("B,H,D,S,cp", FEW_HEAD_SHAPES,
+                         ids=[f"B{c[0]}H{c[1]}D{c[2]}S{c[3]}" for c in FEW_HEAD_SHAPES])
+def test_few_head_shapes(B, H, D, S, cp):
+    g = torch.Generator(device="cuda").manual_seed(B * 7919 + H * 31 + D + S)
+    if cp is None:
+        cp = [int(x) for x in np.random.default_rng(B + S).integers(0, S, B)]
+    q, k, v = rand_f16(g, (B, H, D)), rand_f16(g, (B, S, H, D)), rand_f16(g, (B, S, H, D))
+    out = dattn.decode(q, k, v, cur_pos_tensor(cp))
+    torch.cuda.synchronize()
+    ref = oracle.decode_f64(to_np(q), to_np(k), to_np(v), np.asarray(cp, np.uint32))
+    plan = dattn.dattn_decode_plan(B, H, D, S)
+    assert_decode_close(out, ref, f"B={B} H={H} D={D} S={S} plan={plan}")

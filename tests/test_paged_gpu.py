@@ -142,3 +142,24 @@ def test_paged_ragged_workload_shape():
     assert torch.equal(out.view(torch.int16), dense.view(torch.int16))
     ref = oracle.decode_f64(to_np(x["q"]), to_np(x["k"]), to_np(x["v"]), x["cur_pos_host"])
     assert_decode_close(out, ref, "paged ragged")
+
+
+# few heads in small pages over long contexts: a page is a small copy, a
+# stage spans many pages and the pre-wait prefetch window many table entries
+# (read one lane per page); B, H, D, page_size, max_pages, current_pos
+FEW_HEAD_CASES = [
+    (1, 1, 128, 16, 8192, [100000]),
+    (1, 2, 128, 16, 8192, [131071]),
+    (4, 1, 128, 16, 4096, [65535, 30000, 1, 50000]),
+    (2, 4, 64, 8, 4096, [32767, 20000]),
+]
+
+
+@pytest.mark.parametrize("B,H,D,ps,maxp,cp", FEW_HEAD_CASES,
+                         ids=[f"B{c[0]}H{c[1]}D{c[2]}ps{c[3]}x{c[4]}" for c in FEW_HEAD_CASES])
+def test_few_heads_small_pages_long_context(B, H, D, ps, maxp, cp):
+    q, kp, vp, table = make_paged(B * 1000 + H * 10 + ps, B, H, D, ps, maxp, share=False)
+    out = dattn.decode_paged(q, kp, vp, torch.from_numpy(table).cuda(), cur_pos_tensor(cp))
+    torch.cuda.synchronize()
+    ref = oracle.decode_paged_f64(to_np(q), to_np(kp), to_np(vp), table, np.asarray(cp, np.uint32))
+    assert_decode_close(out, ref, f"B={B} H={H} ps={ps}")
